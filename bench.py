@@ -1,0 +1,415 @@
+"""Benchmark of the load-balanced block-sparse attention forward path on GB300.
+
+One step = one pass of the whole hot path over the LLM-heads workload
+(B=1, H=32, S=8192, d=128, block=128, causal; 16 global heads Bernoulli(0.9)
+below the diagonal, 16 local heads = window of 4 blocks + block-0 sink):
+mask loads -> LPT plan over (b, h, q-block) items, one worker per SM ->
+block-sparse attention forward (bf16 out + fp32 LSE).
+
+Metric: effective TFLOP/s over computed dense blocks, 4 * block^2 * d FLOP per
+dense block (diagonal blocks counted in full), reported with its fraction of the
+measured bf16 dense tensor-core peak and the per-worker (per-SM) busy-time skew.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+With N > 1 (torchrun, one rank per GPU) every rank runs the same workload as an
+independent replica (weak scaling; the path has no exchange step).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "llm"
+METRIC = "block-sparse attn fwd TFLOP/s on dense blocks, % of bf16 TC peak, SM skew"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_description(w):
+    return (f"{w.name}: B={w.B} H={w.H} S={w.S} d={w.d} block={w.block} causal={int(w.causal)}; "
+            "heads 0-15 Bernoulli(0.9) below the diagonal + diagonal, heads 16-31 window of 4 "
+            "blocks + block-0 sink; Q/K/V bf16 N(0,1)")
+
+
+def dense_blocks(mask_np, causal):
+    m = mask_np != 0
+    if causal:
+        m = m & np.tril(np.ones(m.shape[-2:], dtype=bool))
+    return int(m.sum())
+
+
+def diag_blocks(mask_np):
+    n = min(mask_np.shape[-2:])
+    return int((mask_np[..., np.arange(n), np.arange(n)] != 0).sum())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def time_oracle(w, mask_np, q, k, v, heads, budget_s=None):
+    """Oracle (fp64 CPU) on whole heads of the workload; returns (seconds, effective FLOP)."""
+    from oracle import attention as OA
+
+    flop_per_block = 4.0 * w.block * w.block * w.d
+    t0 = time.perf_counter()
+    flop = 0.0
+    done = []
+    for (b, h) in heads:
+        qh = q[b:b + 1, h:h + 1].double().numpy()
+        kh = k[b:b + 1, h:h + 1].double().numpy()
+        vh = v[b:b + 1, h:h + 1].double().numpy()
+        OA.attention_head(qh, kh, vh, mask_np[b:b + 1, h:h + 1], 0, 0, w.block, w.causal)
+        flop += flop_per_block * dense_blocks(mask_np[b:b + 1, h:h + 1], w.causal)
+        done.append((b, h))
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    return time.perf_counter() - t0, flop, done
+
+
+def cpu_baseline(w, mask_np):
+    """Bounded sample of the oracle on the host cores: 2 global + 2 local heads."""
+    import torch
+
+    from load_balancing_gb300 import workloads as W
+
+    cores = len(os.sched_getaffinity(0))
+    q, k, v = W.make_qkv(W.custom("cpu_sample", 1, 4, w.S, w.d, w.block, w.causal, 0, w.qkv_seed), "cpu")
+    heads_src = [0, 1, 16, 17]
+    sub_mask = np.ascontiguousarray(mask_np[:, heads_src])
+    secs, flop, done = time_oracle(w, sub_mask, q, k, v, [(0, i) for i in range(4)], budget_s=30.0)
+    return {"value": flop / secs / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "torch_threads": torch.get_num_threads(),
+            "sample": f"fp64 numpy oracle on {len(done)} whole heads (2 global, 2 local) of the {w.name} "
+                      f"workload, {secs:.1f} s; dense-block FLOP / wall time"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    import torch
+
+    from load_balancing_gb300 import workloads as W
+    from oracle import loads as OL
+    from oracle import lpt as OP
+
+    w = W.WORKLOADS[WORKLOAD]
+    mask_np = W.make_mask(w)
+    q, k, v = W.make_qkv(W.custom("ref_sample", 1, 2, w.S, w.d, w.block, w.causal, 0, w.qkv_seed), "cpu")
+    cores = len(os.sched_getaffinity(0))
+    sample_heads = [0, 16]  # one global and one local head per step
+    sub_mask = np.ascontiguousarray(mask_np[:, sample_heads])
+    m = 148
+
+    def step():
+        t0 = time.perf_counter()
+        row, _, _ = OL.block_mask_loads(mask_np)
+        OP.lpt_plan(row.reshape(-1), m)
+        _, flop, _ = time_oracle(w, sub_mask, q, k, v, [(0, 0), (0, 1)])
+        return time.perf_counter() - t0, flop
+
+    for _ in range(args.warmup):
+        step()
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        t, f = step()
+        tot_t += t
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_description(w)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: oracle mask loads and textbook LPT over the full workload "
+                                       f"({w.n_items} items, m={m}) plus fp64 attention of 2 whole heads "
+                                       "(1 global, 1 local); FLOP = dense blocks of those heads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+
+    from load_balancing_gb300 import dbsp
+    from load_balancing_gb300 import path as P
+    from load_balancing_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dbsp.library()  # fail loudly now if the library is missing
+
+    w = W.WORKLOADS[WORKLOAD]
+    mask_np = W.make_mask(w)
+    n_dense = dense_blocks(mask_np, w.causal)
+    n_diag = diag_blocks(mask_np) if w.causal else 0
+    flop_per_block = 4.0 * w.block * w.block * w.d
+    flop = flop_per_block * n_dense
+    flop_fa = flop - 0.5 * flop_per_block * n_diag  # diagonal blocks counted as half
+    mask = torch.from_numpy(mask_np).to(dev)
+    q, k, v = W.make_qkv(w, dev)
+    n_workers = P.default_workers(dev)
+    plan_buf = P.alloc_plan(w.B, w.H, w.nQ, w.nK, n_workers, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    timing = torch.zeros(3 * n_workers, dtype=torch.int64, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MiB > L2
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e:
+            e[0].record(stream)
+        dbsp.dbsp_block_mask_loads(mask, plan_buf.row_loads, plan_buf.col_loads, plan_buf.head_loads,
+                                   stream=stream)
+        dbsp.dbsp_plan_lpt(plan_buf.row_loads.view(-1), n_workers, plan_buf.worker_of, plan_buf.worker_offsets,
+                           plan_buf.worklist, plan_buf.worker_loads, stream=stream)
+        if e:
+            e[1].record(stream)
+        dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, plan_buf.worker_offsets,
+                                        plan_buf.worklist, n_workers, out=out, lse=lse, cta_timing=timing,
+                                        stream=stream)
+        if e:
+            e[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    status = dbsp.dbsp_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    skews = []
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush, outside the timed events
+        step(ev[i])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop() if rank == 0 else None
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    plan_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    total_s = sum(step_ms) / 1e3
+    total_s = max_over_ranks(total_s, world, dev)
+    t = timing.view(n_workers, 3).cpu().numpy()
+    busy = (t[:, 1] - t[:, 0]).astype(np.float64)
+    skew = float((busy.max() - busy.mean()) / busy.mean())
+    blocks_per_worker = t[:, 2]
+    status = dbsp.dbsp_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # end to end through the public API, host (pinned) buffers in and out
+    q_h, k_h, v_h = (x.cpu().pin_memory() for x in (q, k, v))
+    mask_h = torch.from_numpy(mask_np).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, mask_h))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def e2e_step(e=None):
+        if e:
+            e[0].record(stream)
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        mask.copy_(mask_h, non_blocking=True)
+        p = P.plan(mask, n_workers, out=plan_buf, stream=stream)
+        P.attention(q, k, v, mask, w.block, w.causal, p, out=out, lse=lse, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        if e:
+            e[1].record(stream)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_step(e2e_ev[i])
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3, world, dev)
+
+    total_flop = sum_over_ranks(flop * args.steps, world, dev)
+    value = total_flop / total_s / 1e12
+    attn_avg_s = statistics.mean(attn_ms) / 1e3
+    attn_tflops = flop / attn_avg_s / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_description(w), "n_workers": n_workers, "worklist": "LPT (device)",
+                   "dense_blocks": n_dense, "items": w.n_items,
+                   "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "attn_tflops": attn_tflops,
+        "attn_tflops_fa_convention": flop_fa / attn_avg_s / 1e12,
+        "pct_of_bf16_peak": 100.0 * attn_tflops / peak,
+        "sm_skew": skew,
+        "blocks_per_worker": {"min": int(blocks_per_worker.min()), "max": int(blocks_per_worker.max()),
+                              "mean": float(blocks_per_worker.mean())},
+        "loads_plus_plan_us": 1e3 * statistics.mean(plan_ms),
+        "attn_us": 1e6 * attn_avg_s,
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": attn_tflops / peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 dense (burst, cuBLAS)",
+                     "kernel": "attn_fwd_kernel<128,128>"},
+        "e2e": {"value": total_flop / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "wall_s_timed": wall,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, mask_np)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["dbsp", "reference"], default="dbsp")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

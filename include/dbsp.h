@@ -1,0 +1,171 @@
+/*
+ * dbsp.h -- C ABI of libdbsp.so: load-balanced block-sparse attention forward on
+ * one GB300 (sm_103a).
+ *
+ * The operations follow two web pages:
+ *   [db-SP blog]  "db-SP：稀疏注意力头并行和序列并行的负载均衡问题"
+ *                 (yjmstr.github.io, 2026-01-30), scenarios 1 and 2;
+ *   [6D notes]    "6D 并行下的 Attention Kernel 与通信重叠" (walkerchi.com),
+ *                 §2.1 ring-attention pseudocode and §2.3 causal / striped.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are caller-owned DEVICE memory unless stated otherwise (e.g. a torch
+ *   tensor's data_ptr()). The library never frees or keeps them, and allocates no
+ *   device memory per call. It keeps one device error word per device (a static
+ *   __device__ variable) and caches nothing else that refers to caller memory.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream). Every call only
+ *   enqueues work on it and returns; results are ready when the stream is.
+ * - Arguments are validated on the host before anything touches the GPU:
+ *   DBSP_ERR_INVALID_ARG for a bad size, NULL or misaligned pointer,
+ *   DBSP_ERR_UNSUPPORTED for a shape the kernels do not implement or a device
+ *   that is not sm_103, DBSP_ERR_CUDA for a failed launch (the CUDA error is
+ *   cleared and its text is kept for dbsp_last_error_string()).
+ * - Problems the kernels can only see in device data (a negative load, an item
+ *   id out of range in a worklist, a pipeline wait that timed out) set the
+ *   device error word instead of faulting; dbsp_device_status() reports it.
+ * - Integer outputs are exact; there is exactly one correct worklist.
+ * - No CPU fallback exists: every call either launches its kernel or fails.
+ */
+#ifndef DBSP_H
+#define DBSP_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DBSP_API __attribute__((visibility("default")))
+#else
+#define DBSP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DBSP_OK = 0,
+  DBSP_ERR_INVALID_ARG = 1,
+  DBSP_ERR_UNSUPPORTED = 2,
+  DBSP_ERR_CUDA = 3,
+  DBSP_ERR_TIMEOUT = 4
+} dbsp_status;
+
+/* Largest worker count dbsp_plan_lpt accepts (one warp holds 32 loads per lane). */
+#define DBSP_MAX_WORKERS 1024
+
+/* Static text for a status code. Never NULL. */
+DBSP_API const char* dbsp_status_string(int status);
+
+/* Text of the last DBSP_ERR_CUDA raised on the calling thread ("" if none). */
+DBSP_API const char* dbsp_last_error_string(void);
+
+/*
+ * Mask loads.  [db-SP blog, scenario 2, first bullet]: the load of a Q-block is
+ * the number of dense (non-zero) blocks in its row of the head's block mask, the
+ * load of a KV-block the number in its column. [db-SP blog, scenario 1]: a head's
+ * load is its total number of dense blocks.
+ *
+ *   mask        uint8 [B, H, nQ, nK], row-major; any non-zero byte is dense.
+ *   row_loads   int32 [B, H, nQ]  out: dense blocks per Q-block row.
+ *   col_loads   int32 [B, H, nK]  out: dense blocks per KV-block column.
+ *   head_loads  int32 [B, H]      out, may be NULL.
+ * Requires B, H, nQ, nK >= 1 and B*H*nQ*nK < 2^31. Output buffers must not
+ * overlap the mask. Exact integer results; one kernel launch.
+ */
+DBSP_API int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK,
+                          int32_t* row_loads, int32_t* col_loads, int32_t* head_loads,
+                          void* stream);
+
+/*
+ * LPT plan with stay-in-place bonus.  [db-SP blog, scenario 1]: repeatedly give
+ * the largest remaining item to the currently least-loaded worker (LPT).
+ * [db-SP blog, scenario 2, third bullet]: an item placed on its original worker
+ * counts as lighter when choosing.
+ *
+ * Items are taken in order of load descending, equal loads by id ascending. Item
+ * i goes to the worker p minimising (L_p - stay_bonus * [p == home[i]], p); then
+ * L_p += loads[i] (the true load). Ties go to the lowest worker index.
+ *
+ *   loads          int32 [n_items], each >= 0.
+ *   home           int32 [n_items] with values in [0, n_workers), or NULL (no bonus).
+ *   n_items        >= 0;  n_workers in [1, DBSP_MAX_WORKERS];  stay_bonus >= 0.
+ *   worker_of      int32 [n_items]      out: worker of each item.
+ *   worker_offsets int32 [n_workers+1]  out: CSR offsets into worklist.
+ *   worklist       int32 [n_items]      out: item ids grouped by worker, each
+ *                                       group in assignment order.
+ *   worker_loads   int64 [n_workers]    out, may be NULL: accrued true loads.
+ * Limits: n_items * n_workers < 2^31; either max(loads) <= 32767 or
+ * n_items <= 16384 (otherwise the device error word is set to
+ * DBSP_ERR_UNSUPPORTED). A negative load or out-of-range home sets
+ * DBSP_ERR_INVALID_ARG on the device. One single-CTA kernel launch; the output
+ * arrays double as the kernel's working storage.
+ */
+DBSP_API int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
+                  int32_t stay_bonus, int32_t* worker_of, int32_t* worker_offsets,
+                  int32_t* worklist, int64_t* worker_loads, void* stream);
+
+/*
+ * Block-sparse attention forward over an LPT worklist.  [6D notes §2.1, step 2]:
+ * a chunk of keys yields the unnormalised output O, the row maximum m and the
+ * row sum l of the softmax numerators; the result is O / l (last line of the
+ * loop). Keys are admitted only in dense blocks of the mask ([db-SP blog,
+ * scenario 2]); with causal != 0 a query sees keys at or before its position
+ * ([6D notes §2.3]), blocks above the diagonal are skipped and the diagonal
+ * block is masked element-wise.
+ *
+ *   q, k, v     bf16 [B, H, S, d] contiguous, 16-byte aligned.
+ *   mask        uint8 [B, H, nQ, nK], nQ = nK = S / block.
+ *   d in {64, 128}; block in {64, 128}; S % block == 0.
+ *   scale       softmax scale; <= 0 selects 1/sqrt(d).
+ *   worker_offsets, worklist, n_workers: a CSR worklist over items
+ *               id = (b*H + h)*nQ + qb, e.g. from dbsp_plan_lpt. One CTA runs per
+ *               worker, in list order. Items missing from the worklist are not
+ *               written; an out-of-range id sets DBSP_ERR_INVALID_ARG on the device.
+ * Final mode (out != NULL, o_part == NULL):
+ *   out         bf16 [B, H, S, d]: O / l, rounded to nearest even.
+ *   lse         fp32 [B, H, S] or NULL: m + ln(l) in natural-log units; rows with
+ *               no admissible key get O = 0 and lse = -inf.
+ * Partial mode (out == NULL; o_part, m_part, l_part all non-NULL; lse ignored):
+ *   o_part      fp32 [B, H, S, d]: unnormalised O relative to the row maximum.
+ *   m_part      fp32 [B, H, S]: row maximum of the scaled scores (-inf if empty).
+ *   l_part      fp32 [B, H, S]: row sum of exp(score - m) (0 if empty).
+ * cta_timing    int64 [n_workers * 3] or NULL: per worker the %globaltimer (ns)
+ *               at start and end and the number of dense blocks processed.
+ * Arithmetic: bf16 inputs, fp32 accumulation on the tensor cores; probabilities
+ * are rounded to bf16 before the P.V product.
+ */
+DBSP_API int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const void* v,
+                               const uint8_t* mask, int B, int H, int S, int d, int block,
+                               int causal, float scale,
+                               const int32_t* worker_offsets, const int32_t* worklist,
+                               int n_workers,
+                               void* out, float* lse,
+                               float* o_part, float* m_part, float* l_part,
+                               int64_t* cta_timing, void* stream);
+
+/*
+ * Merge of KV-shard partials.  [6D notes §2.1, step 3 and the final division]:
+ * m* = max_k m_k, l = sum_k exp(m_k - m*) l_k, O = sum_k exp(m_k - m*) O_k / l.
+ * A partial with l_k == 0 or m_k == -inf contributes nothing; a row whose
+ * partials are all empty gets O = 0 and lse = -inf.
+ *
+ *   o_parts  fp32 [n_shards, rows, d];  m_parts, l_parts fp32 [n_shards, rows].
+ *   out      bf16 [rows, d];  lse fp32 [rows] or NULL.
+ * n_shards >= 1, rows >= 0, d a multiple of 4 in [4, 1024], 16-byte aligned
+ * o_parts and 8-byte aligned out.
+ */
+DBSP_API int dbsp_merge_partials(const float* o_parts, const float* m_parts, const float* l_parts,
+                        int n_shards, int64_t rows, int d, void* out, float* lse,
+                        void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error word
+ * (DBSP_OK if no kernel reported a problem since the last call).
+ */
+DBSP_API int dbsp_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DBSP_H */

@@ -15,7 +15,8 @@ __all__ = ["workloads", "dbsp"]
 
 
 def __getattr__(name):
-    if name == "dbsp":
-        from . import dbsp
-        return dbsp
+    if name in ("dbsp", "path", "build"):
+        import importlib
+
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

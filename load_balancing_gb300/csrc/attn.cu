@@ -1,0 +1,639 @@
+// Block-sparse attention forward over an LPT worklist, for sm_103a.
+//
+// What is computed (6D attention notes §2.1, step 2 and the final division; db-SP
+// blog, scenario 2): for every item (b, h, qb) the query rows of Q-block qb attend
+// to the keys of the dense KV-blocks of mask row (b, h, qb); the result is the
+// online-softmax accumulation O / l with LSE = m + ln l, or the unnormalised
+// partial (O, m, l) of one KV shard. Causal (6D attention notes §2.3): blocks
+// above the diagonal are skipped and the diagonal block is masked per element.
+//
+// Design (one persistent CTA per worker, 6 warps):
+//   warp 0      producer: scans the item's mask row with ballots, publishes the
+//               item (id, dense count) and issues TMA loads of the Q tile and of
+//               ONLY the dense K/V tiles into a ring of shared-memory stages, in
+//               the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
+//   warp 1      TMEM owner (512 columns); lane 0 issues tcgen05.mma:
+//               S = Q K^T into one of two TMEM S buffers, O += P V into the TMEM
+//               accumulator, each batch committed to an mbarrier.
+//   warps 2..5  softmax: thread = query row (TMEM lane). tcgen05.ld of the S row,
+//               diagonal masking, running max / sum in registers (base-2 units),
+//               P = exp2(S*scale*log2e - m) rounded to bf16 into shared memory in
+//               the 128-byte-swizzled K-major layout the MMA reads; the O
+//               accumulator is rescaled in TMEM only when a row's maximum grows by
+//               more than 2^8 (the result is exact either way: O and l always
+//               share one reference maximum). Then the epilogue (O / l, LSE or the
+//               partial triple with the true row maximum).
+// Pipelining: S(j+1) is computed while the softmax of block j runs; PV(j) runs
+// while the softmax of block j+1 runs.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer). On expiry the CTA sets the
+// device error word to DBSP_ERR_TIMEOUT, every role leaves its loop, in-flight
+// copies and MMAs are waited for (bounded) and TMEM is freed before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace dbsp::ptx;
+
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
+constexpr uint64_t kDrainLimitNs = 100000000ull;    // 100 ms per teardown wait
+constexpr float kRescaleThreshold = 8.0f;           // log2 units: P <= 256 between rescales
+
+struct AttnParams {
+  const uint8_t* mask;
+  int H, S, nQ, nK, n_items;
+  int causal;
+  float scale_log2;
+  const int32_t* offsets;
+  const int32_t* worklist;
+  __nv_bfloat16* out;
+  float* lse;
+  float* o_part;
+  float* m_part;
+  float* l_part;
+  int64_t* timing;
+  int* err;
+};
+
+template <int BLOCK, int D>
+struct Cfg {
+  static constexpr int kM = 128;                          // MMA rows (query tile)
+  static constexpr int kChunk128 = 128 * 128;             // 128 rows x 128 B
+  static constexpr int kQBytes = (D / 64) * kChunk128;
+  static constexpr int kPBytes = (BLOCK / 64) * kChunk128;
+  static constexpr int kTileChunk = BLOCK * 128;          // BLOCK rows x 128 B
+  static constexpr int kTileBytes = (D / 64) * kTileChunk;
+  static constexpr int kTx = BLOCK * D * 2;               // bytes per Q / K / V tile load
+  static constexpr int kBudget = 200 * 1024;
+  static constexpr int kStagesFit = (kBudget - kQBytes - kPBytes) / kTileBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kDataBytes = kQBytes + kPBytes + kStages * kTileBytes;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(kM, BLOCK, 0, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(kM, D, 0, 1);
+  static_assert(kStages >= 2, "ring too small");
+};
+
+struct alignas(8) Ctrl {
+  uint64_t q_full, q_empty;
+  uint64_t ring_full[8], ring_empty[8];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done;
+  uint64_t item_full[2], item_empty[2];
+  uint64_t drain;
+  int item_id[2], item_n[2], item_diag[2];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+  long long blocks_done;
+};
+
+template <int BLOCK, int D>
+constexpr size_t smem_bytes() {
+  size_t s = 1024 + Cfg<BLOCK, D>::kDataBytes + sizeof(Ctrl) + 64;
+  return s < 136 * 1024 ? 136 * 1024 : s;  // one CTA (one TMEM owner) per SM; slack after the ring
+}
+
+// Bounded wait. Returns false on timeout or when another role has aborted.
+__device__ __forceinline__ bool wait_bar(Ctrl* c, uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (c->abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        c->abort_flag = 1;
+        dbsp::report(err, DBSP_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Teardown wait: ignores the abort flag, short limit, no error on success.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kDrainLimitNs) break;
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ producer
+template <int BLOCK, int D>
+__device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                             const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sRing, int worker) {
+  using C = Cfg<BLOCK, D>;
+  const int lane = threadIdx.x & 31;
+  int begin = p.offsets[worker], end = p.offsets[worker + 1];
+  if (begin < 0 || end < begin) {
+    if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+    begin = end = 0;
+  }
+  uint32_t item_cnt = 0, q_cnt = 0, ring_cnt = 0;
+  bool ok = true;
+  // q/k/v tile issue (lane 0 only)
+  auto issue_tile = [&](const CUtensorMap* map, int row) -> bool {
+    const uint32_t s = ring_cnt % C::kStages, u = ring_cnt / C::kStages;
+    const uint32_t full = smem_u32(&c->ring_full[s]);
+    if (!wait_bar(c, smem_u32(&c->ring_empty[s]), (u & 1) ^ 1, p.err)) return false;
+    mbar_arrive_expect_tx(full, C::kTx);
+    const uint32_t dst = smem_u32(sRing + s * C::kTileBytes);
+#pragma unroll
+    for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kTileChunk, map, ch * 64, row, full);
+    ++ring_cnt;
+    return true;
+  };
+
+  for (int idx = begin; idx <= end && ok; ++idx) {
+    int item = -1;
+    if (idx < end) {
+      item = p.worklist[idx];
+      if (item < 0 || item >= p.n_items) {
+        if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+        continue;
+      }
+    }
+    int n = 0, diag = 0, limit = 0;
+    const uint8_t* row = nullptr;
+    long long kv_row0 = 0;
+    if (item >= 0) {
+      const int qb = item % p.nQ;
+      const long long bh = item / p.nQ;
+      kv_row0 = bh * p.S;
+      row = p.mask + (long long)item * p.nK;
+      limit = p.causal ? min(p.nK, qb + 1) : p.nK;
+      for (int c0 = 0; c0 < limit; c0 += 128) {
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int col = c0 + 32 * uu + lane;
+          const bool dense = col < limit && row[col] != 0;
+          n += __popc(__ballot_sync(0xffffffffu, dense));
+        }
+      }
+      diag = p.causal && row[qb] != 0;
+    }
+    // publish the item
+    const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
+    if (lane == 0) {
+      ok = wait_bar(c, smem_u32(&c->item_empty[slot]), (su & 1) ^ 1, p.err);
+      if (ok) {
+        c->item_id[slot] = item;
+        c->item_n[slot] = n;
+        c->item_diag[slot] = diag;
+        mbar_arrive(smem_u32(&c->item_full[slot]));
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    ++item_cnt;
+    if (!ok || item < 0) break;
+    if (n == 0) continue;
+    if (lane == 0) {
+      ok = wait_bar(c, smem_u32(&c->q_empty), (q_cnt & 1) ^ 1, p.err);
+      if (ok) {
+        const uint32_t full = smem_u32(&c->q_full);
+        mbar_arrive_expect_tx(full, C::kTx);
+        const int qrow = (int)(kv_row0 + (long long)(item % p.nQ) * BLOCK);
+#pragma unroll
+        for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(smem_u32(sQ + ch * C::kChunk128), tq, ch * 64, qrow, full);
+      }
+      ++q_cnt;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    int prev = -1;
+    for (int c0 = 0; c0 < limit && ok; c0 += 128) {
+      unsigned bits[4];
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu) {
+        const int col = c0 + 32 * uu + lane;
+        bits[uu] = __ballot_sync(0xffffffffu, col < limit && row[col] != 0);
+      }
+      if (lane == 0) {
+        for (int uu = 0; uu < 4 && ok; ++uu) {
+          unsigned b = bits[uu];
+          while (b && ok) {
+            const int col = c0 + 32 * uu + (__ffs(b) - 1);
+            b &= b - 1;
+            ok = issue_tile(tk, (int)(kv_row0 + (long long)col * BLOCK));
+            if (ok && prev >= 0) ok = issue_tile(tv, (int)(kv_row0 + (long long)prev * BLOCK));
+            prev = col;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (lane == 0 && ok) ok = issue_tile(tv, (int)(kv_row0 + (long long)prev * BLOCK));
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+  }
+  // teardown: let every copy this CTA started land before shared memory goes away
+  if (lane == 0) {
+    const uint32_t issued = ring_cnt;
+    for (uint32_t k = issued > (uint32_t)C::kStages ? issued - C::kStages : 0; k < issued; ++k)
+      drain_bar(smem_u32(&c->ring_full[k % C::kStages]), (k / C::kStages) & 1);
+    if (q_cnt) drain_bar(smem_u32(&c->q_full), (q_cnt - 1) & 1);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int BLOCK, int D>
+__device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sP, uint8_t* sRing,
+                        uint32_t tmem) {
+  using C = Cfg<BLOCK, D>;
+  uint32_t item_cnt = 0, q_cnt = 0, ring_cnt = 0, g = 0;
+  long long blocks = 0;
+  bool ok = true;
+  const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), ring_addr = smem_u32(sRing);
+  while (ok) {
+    const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
+    if (!wait_bar(c, smem_u32(&c->item_full[slot]), su & 1, p.err)) break;
+    const int item = c->item_id[slot], n = c->item_n[slot];
+    mbar_arrive(smem_u32(&c->item_empty[slot]));
+    ++item_cnt;
+    if (item < 0) break;
+    if (n == 0) continue;
+    if (!wait_bar(c, smem_u32(&c->q_full), q_cnt & 1, p.err)) break;
+    ++q_cnt;
+    for (int jj = 0; jj <= n && ok; ++jj) {
+      if (jj < n) {  // S(g + jj) = Q K^T
+        const uint32_t gg = g + jj, sb = gg & 1;
+        const uint32_t s = ring_cnt % C::kStages, u = ring_cnt / C::kStages;
+        ok = wait_bar(c, smem_u32(&c->s_free[sb]), ((gg >> 1) & 1) ^ 1, p.err) &&
+             wait_bar(c, smem_u32(&c->ring_full[s]), u & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kt = ring_addr + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(q_addr + (kk >> 2) * C::kChunk128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(kt + (kk >> 2) * C::kTileChunk + (kk & 3) * 32, 16, 1024);
+          mma_bf16_ss(tmem + sb * 128, a, b, C::kIdescS, kk > 0);
+        }
+        mma_commit(smem_u32(&c->ring_empty[s]));
+        mma_commit(smem_u32(&c->s_full[sb]));
+        if (jj == n - 1) mma_commit(smem_u32(&c->q_empty));
+        ++ring_cnt;
+      }
+      if (jj > 0) {  // O (+)= P V for block g + jj - 1
+        const uint32_t gp = g + jj - 1;
+        const uint32_t s = ring_cnt % C::kStages, u = ring_cnt / C::kStages;
+        ok = wait_bar(c, smem_u32(&c->p_full), gp & 1, p.err) &&
+             wait_bar(c, smem_u32(&c->ring_full[s]), u & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vt = ring_addr + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < BLOCK / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * C::kChunk128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(vt + kk * 16 * 128, C::kTileChunk, 1024);
+          mma_bf16_ss(tmem + kOCol, a, b, C::kIdescPV, (jj > 1 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&c->ring_empty[s]));
+        mma_commit(smem_u32(&c->pv_done));
+        ++ring_cnt;
+      }
+    }
+    g += n;
+    blocks += n;
+  }
+  // teardown: every MMA issued by this thread must finish before TMEM is freed
+  mma_commit(smem_u32(&c->drain));
+  drain_bar(smem_u32(&c->drain), 0);
+  c->blocks_done = blocks;
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+template <int BLOCK, int D>
+__device__ void run_softmax(const AttnParams& p, Ctrl* c, uint8_t* sP, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
+  const bool row_ok = r < BLOCK;
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const bool partial = p.o_part != nullptr;
+  uint32_t item_cnt = 0, g = 0;
+  bool ok = true;
+  while (ok) {
+    const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
+    if (!wait_bar(c, smem_u32(&c->item_full[slot]), su & 1, p.err)) break;
+    const int item = c->item_id[slot], n = c->item_n[slot], diag = c->item_diag[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&c->item_empty[slot]));
+    ++item_cnt;
+    if (item < 0) break;
+    const long long bh = item / p.nQ;
+    const int qb = item % p.nQ;
+    const long long grow = bh * p.S + (long long)qb * BLOCK + r;  // global query row
+    if (n == 0) {
+      if (row_ok) {
+        if (partial) {
+          float4* o = reinterpret_cast<float4*>(p.o_part + grow * D);
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.m_part[grow] = -INFINITY;
+          p.l_part[grow] = 0.f;
+        } else {
+          uint4* o = reinterpret_cast<uint4*>(p.out + grow * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse) p.lse[grow] = -INFINITY;
+        }
+      }
+      continue;
+    }
+    float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    for (int jj = 0; jj < n; ++jj, ++g) {
+      const uint32_t sb = g & 1;
+      if (!wait_bar(c, smem_u32(&c->s_full[sb]), (g >> 1) & 1, p.err)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[BLOCK];
+      if constexpr (BLOCK == 128) tmem_ld128_wait(lane_base + sb * 128, sr);
+      else tmem_ld64_wait(lane_base + sb * 128, sr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->s_free[sb]));
+
+      float alpha = 1.f;
+      bool rescale = false;
+      if (row_ok) {
+        float* s = reinterpret_cast<float*>(sr);
+        if (diag && jj == n - 1) {
+#pragma unroll
+          for (int k = 0; k < BLOCK; ++k) if (k > r) s[k] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int k = 1; k < BLOCK; ++k) mx = fmaxf(mx, s[k]);
+        const float mxs = mx * p.scale_log2;
+        m_true = fmaxf(m_true, mxs);
+        if (jj == 0) {
+          m_ref = mxs;
+        } else if (mxs > m_ref + kRescaleThreshold) {
+          alpha = ex2(m_ref - mxs);
+          l *= alpha;
+          m_ref = mxs;
+          rescale = true;
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < BLOCK; ++k) {
+          const float e = ex2(fmaf(s[k], p.scale_log2, -m_ref));
+          s[k] = e;
+          sum += e;
+        }
+        l += sum;
+      }
+      // P and O may be touched only once PV of the previous block is complete
+      if (!wait_bar(c, smem_u32(&c->pv_done), (g & 1) ^ 1, p.err)) { ok = false; break; }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32_wait(lane_base + kOCol + cc * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + kOCol + cc * 32, o);
+        }
+        tmem_wait_st();
+      }
+      if (row_ok) {
+        const float* s = reinterpret_cast<const float*>(sr);
+        uint8_t* prow = sP + r * 128;
+#pragma unroll
+        for (int u = 0; u < BLOCK / 8; ++u) {
+          uint4 v;
+          v.x = pack_bf16(s[8 * u + 0], s[8 * u + 1]);
+          v.y = pack_bf16(s[8 * u + 2], s[8 * u + 3]);
+          v.z = pack_bf16(s[8 * u + 4], s[8 * u + 5]);
+          v.w = pack_bf16(s[8 * u + 6], s[8 * u + 7]);
+          const int chunk = u >> 3, unit = u & 7;
+          *reinterpret_cast<uint4*>(prow + chunk * Cfg<BLOCK, D>::kChunk128 + ((unit ^ (r & 7)) << 4)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->p_full));
+    }
+    if (!ok) break;
+    // epilogue: wait for the last PV of this item
+    if (!wait_bar(c, smem_u32(&c->pv_done), (g - 1) & 1, p.err)) break;
+    tc_fence_after();
+    uint32_t o[D];
+    if constexpr (D == 128) tmem_ld128_wait(lane_base + kOCol, o);
+    else tmem_ld64_wait(lane_base + kOCol, o);
+    tc_fence_before();
+    if (row_ok) {
+      const float* of = reinterpret_cast<const float*>(o);
+      constexpr float kLn2 = 0.693147180559945309f;
+      if (partial) {
+        const float f = ex2(m_ref - m_true);
+        float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D);
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i)
+          dst[i] = make_float4(of[4 * i] * f, of[4 * i + 1] * f, of[4 * i + 2] * f, of[4 * i + 3] * f);
+        p.m_part[grow] = m_true * kLn2;
+        p.l_part[grow] = l * f;
+      } else {
+        const float inv = 1.f / l;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * D);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          uint4 v;
+          v.x = pack_bf16(of[8 * i + 0] * inv, of[8 * i + 1] * inv);
+          v.y = pack_bf16(of[8 * i + 2] * inv, of[8 * i + 3] * inv);
+          v.z = pack_bf16(of[8 * i + 4] * inv, of[8 * i + 5] * inv);
+          v.w = pack_bf16(of[8 * i + 6] * inv, of[8 * i + 7] * inv);
+          dst[i] = v;
+        }
+        if (p.lse) p.lse[grow] = (m_ref + __log2f(l)) * kLn2;
+      }
+    }
+  }
+}
+
+template <int BLOCK, int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __grid_constant__ CUtensorMap tv, const AttnParams p) {
+  using C = Cfg<BLOCK, D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sP = sQ + C::kQBytes;
+  uint8_t* sRing = sP + C::kPBytes;
+  Ctrl* c = reinterpret_cast<Ctrl*>(sRing + C::kStages * C::kTileBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t t_start = globaltimer();
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&c->q_full), 1);
+    mbar_init(smem_u32(&c->q_empty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&c->ring_full[s]), 1);
+      mbar_init(smem_u32(&c->ring_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c->s_full[b]), 1);
+      mbar_init(smem_u32(&c->s_free[b]), 4);
+      mbar_init(smem_u32(&c->item_full[b]), 1);
+      mbar_init(smem_u32(&c->item_empty[b]), 5);
+    }
+    mbar_init(smem_u32(&c->p_full), 4);
+    mbar_init(smem_u32(&c->pv_done), 1);
+    mbar_init(smem_u32(&c->drain), 1);
+    c->abort_flag = 0;
+    c->blocks_done = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem_base;
+
+  if (warp == 0) {
+    run_producer<BLOCK, D>(&tq, &tk, &tv, p, c, sQ, sRing, blockIdx.x);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<BLOCK, D>(p, c, sQ, sP, sRing, tmem);
+    __syncwarp();
+  } else {
+    run_softmax<BLOCK, D>(p, c, sP, tmem);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && p.timing) {
+    p.timing[3 * blockIdx.x + 0] = (int64_t)t_start;
+    p.timing[3 * blockIdx.x + 1] = (int64_t)globaltimer();
+    p.timing[3 * blockIdx.x + 2] = c->blocks_done;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int encode_map(CUtensorMap* map, const void* ptr, long long rows, int d, int block) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return DBSP_ERR_CUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)block};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DBSP_OK : DBSP_ERR_CUDA;
+}
+
+template <int BLOCK, int D>
+int launch_attn(const void* q, const void* k, const void* v, const AttnParams& p, long long rows,
+                int n_workers, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  if (encode_map(&tq, q, rows, D, BLOCK) || encode_map(&tk, k, rows, D, BLOCK) ||
+      encode_map(&tv, v, rows, D, BLOCK))
+    return dbsp::cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  constexpr size_t smem = smem_bytes<BLOCK, D>();
+  auto kernel = attn_fwd_kernel<BLOCK, D>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(attn)");
+  kernel<<<n_workers, kThreads, smem, stream>>>(tq, tk, tv, p);
+  DBSP_LAUNCH_CHECK("launch attn_fwd");
+  return DBSP_OK;
+}
+
+}  // namespace
+
+extern "C" int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const void* v,
+                                          const uint8_t* mask, int B, int H, int S, int d,
+                                          int block, int causal, float scale,
+                                          const int32_t* worker_offsets, const int32_t* worklist,
+                                          int n_workers, void* out, float* lse, float* o_part,
+                                          float* m_part, float* l_part, int64_t* cta_timing,
+                                          void* stream) {
+  if (!q || !k || !v || !mask || !worker_offsets || !worklist) return DBSP_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || n_workers < 1 || n_workers > (1 << 20)) return DBSP_ERR_INVALID_ARG;
+  const bool final_mode = out != nullptr;
+  const bool partial_mode = o_part != nullptr || m_part != nullptr || l_part != nullptr;
+  if (final_mode == partial_mode) return DBSP_ERR_INVALID_ARG;
+  if (partial_mode && (!o_part || !m_part || !l_part)) return DBSP_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || (block != 64 && block != 128)) return DBSP_ERR_UNSUPPORTED;
+  if (S % block != 0) return DBSP_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * H * S;
+  const long long n_items = (long long)B * H * (S / block);
+  if (rows >= (1LL << 31) || n_items * (S / block) >= (1LL << 40)) return DBSP_ERR_INVALID_ARG;
+  if (!dbsp::aligned(q, 16) || !dbsp::aligned(k, 16) || !dbsp::aligned(v, 16) ||
+      (out && !dbsp::aligned(out, 16)) || (o_part && !dbsp::aligned(o_part, 16)) ||
+      (lse && !dbsp::aligned(lse, 4)) || (m_part && !dbsp::aligned(m_part, 4)) ||
+      (l_part && !dbsp::aligned(l_part, 4)) || (cta_timing && !dbsp::aligned(cta_timing, 8)))
+    return DBSP_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = dbsp::check_device(&dev);
+  if (st != DBSP_OK) return st;
+  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)d);
+
+  AttnParams p;
+  p.mask = mask;
+  p.H = H;
+  p.S = S;
+  p.nQ = S / block;
+  p.nK = S / block;
+  p.n_items = (int)n_items;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.offsets = worker_offsets;
+  p.worklist = worklist;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = final_mode ? lse : nullptr;
+  p.o_part = o_part;
+  p.m_part = m_part;
+  p.l_part = l_part;
+  p.timing = cta_timing;
+  p.err = dbsp::error_word(dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (block == 128 && d == 128) return launch_attn<128, 128>(q, k, v, p, rows, n_workers, s);
+  if (block == 128 && d == 64) return launch_attn<128, 64>(q, k, v, p, rows, n_workers, s);
+  if (block == 64 && d == 128) return launch_attn<64, 128>(q, k, v, p, rows, n_workers, s);
+  return launch_attn<64, 64>(q, k, v, p, rows, n_workers, s);
+}

@@ -1,0 +1,90 @@
+// Merge of (O, m, l) partials from KV shards into the final output.
+//
+// 6D attention notes §2.1, step 3 of the ring loop and its last line: the running
+// maximum is the larger maximum, each side is rescaled by exp(old max - new max),
+// row sums and unnormalised outputs add with those weights, and the output is
+// divided by the row sum at the end. Folding n shards that way equals the
+// one-shot form m* = max_k m_k, w_k = exp(m_k - m*), l = sum w_k l_k,
+// O = sum w_k O_k / l, which this kernel evaluates (fewer dependent steps).
+// A partial with l_k == 0 or m_k == -inf is empty and contributes nothing.
+//
+// Layout: o_parts [n_shards, rows, d] fp32, m/l [n_shards, rows] fp32. One thread
+// owns 4 consecutive elements of a row (float4 loads, streaming cache hint,
+// coalesced along d) and writes 4 bf16 (one 8-byte store). HBM-bound: each
+// partial is read exactly once.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) merge_partials_kernel(
+    const float* __restrict__ o_parts, const float* __restrict__ m_parts,
+    const float* __restrict__ l_parts, int n_shards, long long rows, int d,
+    __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  const int quads = d >> 2;
+  const long long total = rows * quads;
+  const long long stride = (long long)gridDim.x * kThreads;
+  for (long long u = (long long)blockIdx.x * kThreads + threadIdx.x; u < total; u += stride) {
+    const long long row = u / quads;
+    const int c4 = (int)(u - row * quads);
+    // pass 1: m* over live partials
+    float mstar = -INFINITY;
+    for (int k = 0; k < n_shards; ++k) {
+      const float mk = __ldg(m_parts + (long long)k * rows + row);
+      const float lk = __ldg(l_parts + (long long)k * rows + row);
+      if (lk > 0.f && mk > -INFINITY) mstar = fmaxf(mstar, mk);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
+    if (mstar > -INFINITY) {
+      // pass 2: weighted sums
+      for (int k = 0; k < n_shards; ++k) {
+        const float mk = __ldg(m_parts + (long long)k * rows + row);
+        const float lk = __ldg(l_parts + (long long)k * rows + row);
+        if (!(lk > 0.f && mk > -INFINITY)) continue;
+        const float wk = expf(mk - mstar);
+        const float4 o = __ldcs(reinterpret_cast<const float4*>(o_parts + ((long long)k * rows + row) * d) + c4);
+        l += wk * lk;
+        acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
+      }
+      const float inv = 1.f / l;
+      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    __stcs(reinterpret_cast<uint2*>(out + row * d) + c4, packed);
+    if (lse && c4 == 0) lse[row] = mstar > -INFINITY ? mstar + logf(l) : -INFINITY;
+  }
+}
+
+}  // namespace
+
+extern "C" int dbsp_merge_partials(const float* o_parts, const float* m_parts, const float* l_parts,
+                                   int n_shards, int64_t rows, int d, void* out, float* lse,
+                                   void* stream) {
+  if (n_shards < 1 || rows < 0 || d < 4 || d > 1024 || (d % 4) != 0) return DBSP_ERR_INVALID_ARG;
+  if (rows == 0) return DBSP_OK;
+  if (!o_parts || !m_parts || !l_parts || !out) return DBSP_ERR_INVALID_ARG;
+  if (!dbsp::aligned(o_parts, 16) || !dbsp::aligned(out, 8) || !dbsp::aligned(m_parts, 4) ||
+      !dbsp::aligned(l_parts, 4) || (lse && !dbsp::aligned(lse, 4)))
+    return DBSP_ERR_INVALID_ARG;
+  if ((long long)n_shards * rows * d >= (1LL << 62) / 4) return DBSP_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = dbsp::check_device(&dev);
+  if (st != DBSP_OK) return st;
+  const long long units = rows * (d / 4);
+  const long long want = (units + kThreads - 1) / kThreads;
+  const int blocks = (int)std::min<long long>(want, (long long)dbsp::sm_count(dev) * 8);
+  merge_partials_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      o_parts, m_parts, l_parts, n_shards, rows, d, static_cast<__nv_bfloat16*>(out), lse);
+  DBSP_LAUNCH_CHECK("launch merge_partials");
+  return DBSP_OK;
+}

@@ -1,0 +1,146 @@
+"""Thin ctypes binding of libdbsp.so (declared in include/dbsp.h).
+
+Argument marshalling only: each function checks that the torch tensors it is given
+have the dtype, device and contiguity the C ABI expects, passes their pointers and
+the current CUDA stream, and raises ``DbspError`` on a non-zero status. All
+computation happens in the library's CUDA kernels. If the library has not been
+built the first call raises; there is no fallback.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdbsp.so")
+_lib = None
+
+DBSP_OK = 0
+DBSP_ERR_INVALID_ARG = 1
+DBSP_ERR_UNSUPPORTED = 2
+DBSP_ERR_CUDA = 3
+DBSP_ERR_TIMEOUT = 4
+DBSP_MAX_WORKERS = 1024
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int
+_i64 = ctypes.c_int64
+
+_SIGNATURES = {
+    "dbsp_status_string": (ctypes.c_char_p, [_i32]),
+    "dbsp_last_error_string": (ctypes.c_char_p, []),
+    "dbsp_block_mask_loads": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "dbsp_plan_lpt": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
+    "dbsp_block_sparse_attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                          ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp,
+                                          _vp, _vp]),
+    "dbsp_merge_partials": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp]),
+    "dbsp_device_status": (_i32, [_vp]),
+}
+
+
+class DbspError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        lib = library()
+        msg = lib.dbsp_status_string(status).decode()
+        extra = lib.dbsp_last_error_string().decode() if status == DBSP_ERR_CUDA else ""
+        super().__init__(f"{where}: status {status} ({msg}){': ' + extra if extra else ''}")
+
+
+def library():
+    """The loaded libdbsp.so (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libdbsp.so is not built ({_LIB_PATH}); run "
+                               "load_balancing_gb300.build.build() or __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def _check(status, where):
+    if status != DBSP_OK:
+        raise DbspError(status, where)
+
+
+def _ptr(t, dtype, name, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def dbsp_block_mask_loads(mask, row_loads, col_loads, head_loads=None, stream=None):
+    """mask uint8 [B,H,nQ,nK] -> row_loads int32 [B,H,nQ], col_loads [B,H,nK], head_loads [B,H]."""
+    B, H, nQ, nK = mask.shape
+    st = library().dbsp_block_mask_loads(
+        _ptr(mask, torch.uint8, "mask"), B, H, nQ, nK, _ptr(row_loads, torch.int32, "row_loads"),
+        _ptr(col_loads, torch.int32, "col_loads"), _ptr(head_loads, torch.int32, "head_loads", True),
+        _stream(stream))
+    _check(st, "dbsp_block_mask_loads")
+
+
+def dbsp_plan_lpt(loads, n_workers, worker_of, worker_offsets, worklist, worker_loads=None,
+                  home=None, stay_bonus=0, stream=None):
+    """LPT plan: loads int32 [n] -> worker_of [n], worker_offsets [m+1], worklist [n], worker_loads int64 [m]."""
+    n = loads.numel()
+    st = library().dbsp_plan_lpt(
+        _ptr(loads, torch.int32, "loads"), _ptr(home, torch.int32, "home", True), n, n_workers,
+        int(stay_bonus), _ptr(worker_of, torch.int32, "worker_of"),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        _ptr(worker_loads, torch.int64, "worker_loads", True), _stream(stream))
+    _check(st, "dbsp_plan_lpt")
+
+
+def dbsp_block_sparse_attn_fwd(q, k, v, mask, block, causal, worker_offsets, worklist, n_workers,
+                               out=None, lse=None, o_part=None, m_part=None, l_part=None,
+                               scale=0.0, cta_timing=None, stream=None):
+    """Block-sparse attention forward over a CSR worklist (final or partial mode)."""
+    B, H, S, d = q.shape
+    st = library().dbsp_block_sparse_attn_fwd(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+        _ptr(mask, torch.uint8, "mask"), B, H, S, d, block, int(bool(causal)), float(scale),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        n_workers, _ptr(out, torch.bfloat16, "out", True), _ptr(lse, torch.float32, "lse", True),
+        _ptr(o_part, torch.float32, "o_part", True), _ptr(m_part, torch.float32, "m_part", True),
+        _ptr(l_part, torch.float32, "l_part", True), _ptr(cta_timing, torch.int64, "cta_timing", True),
+        _stream(stream))
+    _check(st, "dbsp_block_sparse_attn_fwd")
+
+
+def dbsp_merge_partials(o_parts, m_parts, l_parts, out, lse=None, stream=None):
+    """o_parts fp32 [n, rows, d], m/l fp32 [n, rows] -> out bf16 [rows, d], lse fp32 [rows]."""
+    n, rows, d = o_parts.shape
+    st = library().dbsp_merge_partials(
+        _ptr(o_parts, torch.float32, "o_parts"), _ptr(m_parts, torch.float32, "m_parts"),
+        _ptr(l_parts, torch.float32, "l_parts"), n, rows, d, _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse", True), _stream(stream))
+    _check(st, "dbsp_merge_partials")
+
+
+def dbsp_device_status(stream=None):
+    """Synchronise the stream and return (and clear) the device error word."""
+    return library().dbsp_device_status(_stream(stream))

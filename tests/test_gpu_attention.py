@@ -1,0 +1,197 @@
+"""dbsp_block_sparse_attn_fwd on the GPU against the fp64 oracle.
+
+Small problems (several tiles, ragged dense-block counts, empty rows, more or fewer
+workers than items) are compared element by element; the tiny and LLM workloads
+in full; the video and imbalance workloads on sampled items (whole light/heavy
+heads where the oracle affords it, plus random and heaviest items) in the launch
+configuration the benchmark uses (one worker per SM, LPT worklist).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from load_balancing_gb300 import path as P
+from load_balancing_gb300 import workloads as W
+from oracle import attention as A
+from parity import assert_rows_close, oracle_item, sample_items, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _gpu_problem(w):
+    mask_np = W.make_mask(w)
+    q, k, v = W.make_qkv(w, DEV)
+    return mask_np, torch.from_numpy(mask_np).to(DEV), q, k, v
+
+
+def _small(block, d, causal, B=2, H=3, nblocks=5, seed=0, density=0.45):
+    w = W.custom(f"small_{block}_{d}_{int(causal)}", B, H, nblocks * block, d, block, causal, seed,
+                 seed + 100, "bernoulli", p=density, numpy_qkv=True)
+    mask_np = W.make_mask(w)
+    mask_np[0, 0, 1, :] = 0          # an item with no dense block at all
+    mask_np[B - 1, H - 1, :, 0] = 1  # a sink column
+    return w, mask_np
+
+
+@pytest.mark.parametrize("block,d", [(128, 128), (64, 64), (128, 64), (64, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n_workers", [1, 7, 200])
+def test_small_problems_elementwise(built_library, cuda_device, block, d, causal, n_workers):
+    w, mask_np = _small(block, d, causal)
+    q, k, v = W.make_qkv(w, "cpu")
+    mask = torch.from_numpy(mask_np).to(DEV)
+    p = P.plan(mask, n_workers)
+    out, lse = P.attention(q.to(DEV), k.to(DEV), v.to(DEV), mask, block, causal, p)
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.dbsp_device_status() == 0
+    o_ref, lse_ref = A.attention(to64(q), to64(k), to64(v), mask_np, block, causal)
+    assert_rows_close(to64(out), o_ref, to64(lse), lse_ref, what=f"small b{block} d{d} c{causal}")
+
+
+def test_tiny_workload_full(built_library, cuda_device):
+    w = W.WORKLOADS["tiny"]
+    mask_np = W.make_mask(w)
+    q, k, v = W.make_qkv(w, "cpu")
+    mask = torch.from_numpy(mask_np).to(DEV)
+    for m in (1, 4, P.default_workers()):
+        p = P.plan(mask, m)
+        out, lse = P.attention(q.to(DEV), k.to(DEV), v.to(DEV), mask, w.block, w.causal, p)
+        o_ref, lse_ref = A.attention(to64(q), to64(k), to64(v), mask_np, w.block, w.causal)
+        assert_rows_close(to64(out), o_ref, to64(lse), lse_ref, what=f"tiny m={m}")
+
+
+def test_llm_workload_full(built_library, cuda_device):
+    w = W.WORKLOADS["llm"]
+    mask_np, mask, q, k, v = _gpu_problem(w)
+    p = P.plan(mask, P.default_workers())
+    out, lse = P.attention(q, k, v, mask, w.block, w.causal, p)
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.dbsp_device_status() == 0
+    for b in range(w.B):
+        for h in range(w.H):
+            r = A.attention_head(to64(q[b:b + 1, h:h + 1]), to64(k[b:b + 1, h:h + 1]),
+                                 to64(v[b:b + 1, h:h + 1]), mask_np[b:b + 1, h:h + 1], 0, 0, w.block,
+                                 w.causal)
+            assert_rows_close(to64(out[b, h]), r["o"], to64(lse[b, h]), r["lse"], what=f"llm head {h}")
+
+
+def _check_sampled(w, mask_np, q, k, v, out, lse, items):
+    for item in items:
+        bh, qb = divmod(item, w.nQ)
+        b, h = divmod(bh, w.H)
+        r = oracle_item(q, k, v, mask_np, b, h, qb, w.block, w.causal)
+        rows = slice(qb * w.block, (qb + 1) * w.block)
+        assert_rows_close(to64(out[b, h, rows]), r["o"], to64(lse[b, h, rows]), r["lse"],
+                          what=f"{w.name} item {item}")
+
+
+def test_video_workload_sampled(built_library, cuda_device):
+    w = W.WORKLOADS["video"]
+    mask_np, mask, q, k, v = _gpu_problem(w)
+    p = P.plan(mask, P.default_workers())
+    out, lse = P.attention(q, k, v, mask, w.block, w.causal, p)
+    head_load = (mask_np != 0).sum(axis=(2, 3))[0]
+    order = np.argsort(head_load, kind="stable")
+    heads = [(0, int(h)) for h in (order[0], order[1], order[-1], order[-2])]
+    items = sample_items(mask_np, 64, 8, seed=3, whole_heads=heads)
+    _check_sampled(w, mask_np, q, k, v, out, lse, items)
+
+
+def test_imbalance_workload_sampled(built_library, cuda_device):
+    w = W.WORKLOADS["imbalance"]
+    mask_np, mask, q, k, v = _gpu_problem(w)
+    p = P.plan(mask, P.default_workers())
+    out, lse = P.attention(q, k, v, mask, w.block, w.causal, p)
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.dbsp_device_status() == 0
+    head_load = (mask_np != 0).sum(axis=(2, 3))[0]
+    order = np.argsort(head_load, kind="stable")
+    items = set(sample_items(mask_np, 48, 8, seed=5))
+    rng = np.random.default_rng(6)
+    for h in (order[0], order[1], order[-1], order[-2]):  # a few items of the extreme heads
+        items |= set((int(h) * w.nQ + rng.choice(w.nQ, 3, replace=False)).tolist())
+    _check_sampled(w, mask_np, q, k, v, out, lse, sorted(items))
+    # cheap whole-output properties: finite, LSE finite (every row has its diagonal)
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(lse).all()
+
+
+def test_result_does_not_depend_on_the_worklist(built_library, cuda_device):
+    from load_balancing_gb300 import dbsp
+
+    w, mask_np = _small(128, 128, True, B=1, H=4, nblocks=6, seed=11)
+    q, k, v = (t.to(DEV) for t in W.make_qkv(w, "cpu"))
+    mask = torch.from_numpy(mask_np).to(DEV)
+    p = P.plan(mask, 5)
+    out_a, lse_a = P.attention(q, k, v, mask, w.block, w.causal, p)
+    n = w.n_items
+    rr = torch.arange(n, dtype=torch.int32, device=DEV).flip(0)  # one worker, reversed order
+    off = torch.tensor([0, n], dtype=torch.int32, device=DEV)
+    out_b = torch.empty_like(out_a)
+    lse_b = torch.empty_like(lse_a)
+    dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, off, rr, 1, out=out_b, lse=lse_b)
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+
+
+@pytest.mark.parametrize("block,d,causal", [(128, 128, True), (64, 64, False)])
+def test_partial_mode(built_library, cuda_device, block, d, causal):
+    from load_balancing_gb300 import dbsp
+
+    w, mask_np = _small(block, d, causal, seed=21)
+    q, k, v = W.make_qkv(w, "cpu")
+    mask = torch.from_numpy(mask_np).to(DEV)
+    p = P.plan(mask, 9)
+    shape = (w.B, w.H, w.S)
+    o_part = torch.empty(shape + (d,), dtype=torch.float32, device=DEV)
+    m_part = torch.empty(shape, dtype=torch.float32, device=DEV)
+    l_part = torch.empty(shape, dtype=torch.float32, device=DEV)
+    P.attention_partial(q.to(DEV), k.to(DEV), v.to(DEV), mask, block, causal, p, o_part, m_part, l_part)
+    assert dbsp.dbsp_device_status() == 0
+    o_ref, m_ref, l_ref = A.attention_partials(to64(q), to64(k), to64(v), mask_np, block, causal)
+    m_g, l_g, o_g = to64(m_part), to64(l_part), to64(o_part)
+    empty = ~np.isfinite(m_ref)
+    assert (m_g[empty] == -np.inf).all() and (l_g[empty] == 0).all() and (o_g[empty] == 0).all()
+    live = ~empty
+    assert np.abs(m_g[live] - m_ref[live]).max() <= 1e-3
+    assert (np.abs(l_g[live] / l_ref[live] - 1) <= 1e-2).all()
+    norm = np.where(live[..., None], o_g / np.where(live, l_g, 1)[..., None], 0)
+    assert_rows_close(norm, np.where(live[..., None], o_ref / np.where(live, l_ref, 1)[..., None], 0),
+                      what="partial normalised")
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_sharded_merge_equals_unsharded(built_library, cuda_device, layout):
+    w = W.WORKLOADS["sharded"]
+    mask_np, mask, q, k, v = _gpu_problem(w)
+    m = P.default_workers()
+    p = P.plan(mask, m)
+    out_ref, lse_ref = P.attention(q, k, v, mask, w.block, w.causal, p)
+    shards = torch.from_numpy(W.shard_masks(mask_np, w.extra["n_shards"], layout)).to(DEV)
+    out, lse, _ = P.sharded_attention(q, k, v, shards, w.block, w.causal, m)
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.dbsp_device_status() == 0
+    # merged vs unsharded GPU output, whole tensors
+    assert_rows_close(to64(out).reshape(-1, w.d), to64(out_ref).reshape(-1, w.d),
+                      to64(lse).reshape(-1), to64(lse_ref).reshape(-1), what=f"merge {layout} vs unsharded")
+    # merged vs the oracle on sampled items
+    items = sample_items(mask_np, 24, 4, seed=8)
+    _check_sampled(w, mask_np, q, k, v, out, lse, items)
+
+
+def test_cta_timing_counts_dense_blocks(built_library, cuda_device):
+    w, mask_np = _small(128, 128, True, seed=31)
+    q, k, v = (t.to(DEV) for t in W.make_qkv(w, "cpu"))
+    mask = torch.from_numpy(mask_np).to(DEV)
+    m = 6
+    p = P.plan(mask, m)
+    timing = torch.zeros(3 * m, dtype=torch.int64, device=DEV)
+    P.attention(q, k, v, mask, w.block, w.causal, p, cta_timing=timing)
+    t = timing.view(m, 3).cpu().numpy()
+    assert (t[:, 1] >= t[:, 0]).all()
+    assert t[:, 2].tolist() == p.worker_loads.cpu().numpy().tolist()

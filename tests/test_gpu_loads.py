@@ -1,0 +1,65 @@
+"""dbsp_block_mask_loads on the GPU: bit-exact against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from load_balancing_gb300 import workloads as W
+from oracle import loads as OL
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(mask_np, with_head=True):
+    from load_balancing_gb300 import dbsp
+
+    dev = torch.device("cuda:0")
+    B, H, nQ, nK = mask_np.shape
+    mask = torch.from_numpy(mask_np).to(dev)
+    row = torch.full((B, H, nQ), -7, dtype=torch.int32, device=dev)
+    col = torch.full((B, H, nK), -7, dtype=torch.int32, device=dev)
+    head = torch.full((B, H), -7, dtype=torch.int32, device=dev) if with_head else None
+    dbsp.dbsp_block_mask_loads(mask, row, col, head)
+    assert dbsp.dbsp_device_status() == 0
+    return row.cpu().numpy(), col.cpu().numpy(), None if head is None else head.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_workload_masks(built_library, cuda_device, name):
+    mask = W.make_mask(W.WORKLOADS[name])
+    row, col, head = _run(mask)
+    r, c, h = OL.block_mask_loads(mask)
+    np.testing.assert_array_equal(row, r)
+    np.testing.assert_array_equal(col, c)
+    np.testing.assert_array_equal(head, h)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (2, 3, 5, 7), (1, 2, 16, 48), (1, 1, 300, 16),
+                                   (2, 2, 1000, 33), (1, 1, 4, 16384), (3, 1, 2048, 64), (1, 5, 9, 8)])
+@pytest.mark.parametrize("density", [0.0, 0.3, 1.0])
+def test_random_masks(built_library, cuda_device, shape, density):
+    rng = np.random.default_rng(hash((shape, density)) % 2**32)
+    vals = rng.integers(1, 256, shape).astype(np.uint8)  # any non-zero byte is dense
+    mask = np.where(rng.random(shape) < density, vals, 0).astype(np.uint8)
+    row, col, head = _run(mask, with_head=shape[0] != 3)
+    r, c, h = OL.block_mask_loads(mask)
+    np.testing.assert_array_equal(row, r)
+    np.testing.assert_array_equal(col, c)
+    if head is not None:
+        np.testing.assert_array_equal(head, h)
+
+
+def test_unaligned_mask_pointer_takes_byte_path(built_library, cuda_device):
+    from load_balancing_gb300 import dbsp
+
+    rng = np.random.default_rng(3)
+    mask_np = (rng.random((1, 2, 64, 64)) < 0.5).astype(np.uint8)
+    buf = torch.zeros(mask_np.size + 1, dtype=torch.uint8, device="cuda:0")
+    buf[1:] = torch.from_numpy(mask_np.reshape(-1)).cuda()
+    mask = buf[1:].view(1, 2, 64, 64)  # 1-byte offset: the 16-byte vector path is not allowed
+    row = torch.empty((1, 2, 64), dtype=torch.int32, device="cuda:0")
+    col = torch.empty_like(row)
+    dbsp.dbsp_block_mask_loads(mask, row, col)
+    r, c, _ = OL.block_mask_loads(mask_np)
+    np.testing.assert_array_equal(row.cpu().numpy(), r)
+    np.testing.assert_array_equal(col.cpu().numpy(), c)

@@ -1,0 +1,98 @@
+"""dbsp_plan_lpt on the GPU: bit-exact against the oracle's textbook LPT."""
+
+import numpy as np
+import pytest
+import torch
+
+from load_balancing_gb300 import workloads as W
+from oracle import loads as OL
+from oracle import lpt as OP
+from conftest import load_golden
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan(loads, m, home=None, bonus=0, check_status=True):
+    from load_balancing_gb300 import dbsp
+
+    dev = torch.device("cuda:0")
+    loads_t = torch.as_tensor(np.asarray(loads, dtype=np.int32)).to(dev)
+    n = loads_t.numel()
+    wo = torch.full((n,), -5, dtype=torch.int32, device=dev)
+    off = torch.full((m + 1,), -5, dtype=torch.int32, device=dev)
+    wl = torch.full((n,), -5, dtype=torch.int32, device=dev)
+    wload = torch.full((m,), -5, dtype=torch.int64, device=dev)
+    home_t = None if home is None else torch.as_tensor(np.asarray(home, dtype=np.int32)).to(dev)
+    dbsp.dbsp_plan_lpt(loads_t, m, wo, off, wl, wload, home=home_t, stay_bonus=bonus)
+    status = dbsp.dbsp_device_status()
+    if check_status:
+        assert status == 0
+    return {"worker_of": wo.cpu().numpy(), "offsets": off.cpu().numpy(), "worklist": wl.cpu().numpy(),
+            "worker_loads": wload.cpu().numpy(), "status": status}
+
+
+def _assert_same(got, ref):
+    for key in ("worker_of", "offsets", "worklist", "worker_loads"):
+        np.testing.assert_array_equal(got[key], np.asarray(ref[key]), err_msg=key)
+
+
+def test_page_counterexample(built_library, cuda_device):
+    g = load_golden("lpt_counterexample.json")
+    got = _plan(g["loads"], g["n_workers"])
+    assert got["worker_loads"].tolist() == [17, 13]
+    assert got["worker_of"].tolist() == [0, 1, 1, 0, 0]
+    _assert_same(got, OP.lpt_plan(g["loads"], 2))
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_workload_item_sets(built_library, cuda_device, name):
+    mask = W.make_mask(W.WORKLOADS[name])
+    row = OL.block_mask_loads(mask)[0].reshape(-1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for m in sorted({1, 7, 32, sms, 1024}):
+        _assert_same(_plan(row, m), OP.lpt_plan(row, m))
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 31, 32, 33, 64, 100, 257, 513, 1024])
+def test_random_instances_with_bonus(built_library, cuda_device, m):
+    rng = np.random.default_rng(m)
+    for n in (0, 1, 5, 33, 1000):
+        loads = rng.integers(0, 100, n)
+        _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+        home = rng.integers(0, m, n)
+        bonus = int(rng.integers(0, 150))
+        _assert_same(_plan(loads, m, home, bonus), OP.lpt_plan(loads, m, home, bonus))
+
+
+def test_static_home_schedule_and_huge_bonus(built_library, cuda_device):
+    rng = np.random.default_rng(9)
+    n, m = 4096, 148
+    loads = rng.integers(1, 64, n)
+    home = (np.arange(n) * m) // n  # contiguous static schedule
+    for bonus in (0, 5, 64, int(loads.sum()) + 1):
+        _assert_same(_plan(loads, m, home, bonus), OP.lpt_plan(loads, m, home, bonus))
+
+
+def test_large_loads_take_comparison_sort(built_library, cuda_device):
+    rng = np.random.default_rng(4)
+    loads = rng.integers(0, 5_000_000, 3000)
+    loads[::7] = loads[3]  # plenty of ties
+    _assert_same(_plan(loads, 37), OP.lpt_plan(loads, 37))
+
+
+def test_more_workers_than_items(built_library, cuda_device):
+    loads = [5, 9, 9, 1, 0, 3]
+    _assert_same(_plan(loads, 10), OP.lpt_plan(loads, 10))
+
+
+def test_bad_inputs_set_device_status(built_library, cuda_device):
+    got = _plan([3, -1, 2], 2, check_status=False)
+    assert got["status"] == 1
+    assert (got["offsets"] == 0).all()
+    got = _plan([3, 1, 2], 2, home=[0, 5, 1], bonus=1, check_status=False)
+    assert got["status"] == 1
+    big = np.full(20000, 40000)
+    got = _plan(big, 4, check_status=False)
+    assert got["status"] == 2
+    # the error word is cleared by the read: a good call afterwards is clean
+    _assert_same(_plan([1, 2, 3], 2), OP.lpt_plan([1, 2, 3], 2))
