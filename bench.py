@@ -45,10 +45,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+MASK_TEXT = {
+    "tiny": "8x8 Bernoulli(0.5) block mask per head, diagonal forced",
+    "llm": "heads 0-15 Bernoulli(0.9) below the diagonal + diagonal, heads 16-31 window of 4 blocks + "
+           "block-0 sink",
+    "video": "16 frames x 1024 tokens; heads 0-11 same-frame blocks, heads 12-23 same in-frame offset, "
+             "OR Bernoulli(rho_h), rho_h ~ U[0.05, 0.40]",
+    "sharded": "full lower-triangular block mask; 8 contiguous / 8 striped KV shards",
+    "imbalance": "per-head density lognormal(ln 0.1, 1) clipped to [1%, 60%], uniform block positions per "
+                 "row, diagonal forced",
+}
+
+
 def workload_description(w):
     return (f"{w.name}: B={w.B} H={w.H} S={w.S} d={w.d} block={w.block} causal={int(w.causal)}; "
-            "heads 0-15 Bernoulli(0.9) below the diagonal + diagonal, heads 16-31 window of 4 "
-            "blocks + block-0 sink; Q/K/V bf16 N(0,1)")
+            f"{MASK_TEXT.get(w.name, w.kind)}; Q/K/V bf16 N(0,1)")
 
 
 def dense_blocks(mask_np, causal):
@@ -396,6 +407,125 @@ def run_gpu(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- suite (all workloads)
+def _time_ms(fn, stream, flush, reps):
+    import torch
+
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def static_worklist(n_items, m, kind, device):
+    """Round-robin (item i -> worker i mod m) or contiguous (equal slices) worklists."""
+    import torch
+
+    ids = np.arange(n_items)
+    owner = ids % m if kind == "round_robin" else (ids * m) // max(1, n_items)
+    order = np.argsort(owner, kind="stable")
+    offsets = np.zeros(m + 1, dtype=np.int32)
+    np.add.at(offsets, owner + 1, 1)
+    offsets = np.cumsum(offsets).astype(np.int32)
+    return (torch.from_numpy(offsets).to(device), torch.from_numpy(order.astype(np.int32)).to(device))
+
+
+def run_suite(args):
+    """One JSON line per workload: each kernel of the path timed on its own."""
+    import torch
+
+    from load_balancing_gb300 import dbsp
+    from load_balancing_gb300 import path as P
+    from load_balancing_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dbsp.library()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peaks, peak_src = load_peaks()
+    reps = max(3, args.steps)
+    names = args.workloads.split(",") if args.workloads else W.ORDER
+    for name in names:
+        w = W.WORKLOADS[name]
+        mask_np = W.make_mask(w)
+        n_dense = dense_blocks(mask_np, w.causal)
+        flop = 4.0 * w.block * w.block * w.d * n_dense
+        mask = torch.from_numpy(mask_np).to(dev)
+        q, k, v = W.make_qkv(w, dev)
+        m = P.default_workers(dev)
+        pb = P.alloc_plan(w.B, w.H, w.nQ, w.nK, m, dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        timing = torch.zeros(3 * m, dtype=torch.int64, device=dev)
+        line = {"suite": True, "workload": workload_description(w), "dense_blocks": n_dense,
+                "items": w.n_items, "n_workers": m}
+        # a1: mask loads
+        loads = lambda: dbsp.dbsp_block_mask_loads(mask, pb.row_loads, pb.col_loads, pb.head_loads, stream=stream)
+        t = _time_ms(loads, stream, flush, reps)
+        nbytes = mask_np.size + 4 * (w.B * w.H * (w.nQ + w.nK + 1))
+        line["mask_loads"] = {"us": 1e3 * t, "GB/s": nbytes / t / 1e6, "bytes": nbytes,
+                              "frac_of_hbm": nbytes / t / 1e6 / float(peaks["hbm_gbs"])}
+        # a2: LPT plan
+        plan = lambda: dbsp.dbsp_plan_lpt(pb.row_loads.view(-1), m, pb.worker_of, pb.worker_offsets, pb.worklist,
+                                          pb.worker_loads, stream=stream)
+        line["lpt_plan"] = {"us": 1e3 * _time_ms(plan, stream, flush, reps)}
+        # a3/a4: attention under three worklists
+        for kind in ("lpt", "round_robin", "contiguous"):
+            if kind == "lpt":
+                off, wl = pb.worker_offsets, pb.worklist
+            else:
+                off, wl = static_worklist(w.n_items, m, kind, dev)
+            fn = lambda: dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, off, wl, m, out=out,
+                                                         lse=lse, cta_timing=timing, stream=stream)
+            t = _time_ms(fn, stream, flush, reps)
+            tt = timing.view(m, 3).cpu().numpy()
+            busy = (tt[:, 1] - tt[:, 0]).astype(np.float64)
+            line[f"attn_{kind}"] = {"us": 1e3 * t, "TFLOP/s": flop / t / 1e9,
+                                   "frac_of_bf16_peak": flop / t / 1e9 / float(peaks["bf16_tflops"]),
+                                   "sm_skew": float((busy.max() - busy.mean()) / busy.mean()),
+                                   "blocks_max_over_mean": float(tt[:, 2].max() / max(1e-9, tt[:, 2].mean()))}
+        # a5: merge of KV-shard partials (sharded workload)
+        if "n_shards" in w.extra:
+            n_sh = w.extra["n_shards"]
+            for layout in ("contiguous", "striped"):
+                shards = torch.from_numpy(W.shard_masks(mask_np, n_sh, layout)).to(dev)
+                o_p = torch.empty((n_sh, w.B, w.H, w.S, w.d), dtype=torch.float32, device=dev)
+                m_p = torch.empty((n_sh, w.B, w.H, w.S), dtype=torch.float32, device=dev)
+                l_p = torch.empty_like(m_p)
+                plans = [P.plan(shards[s], m) for s in range(n_sh)]
+
+                def partials():
+                    for s in range(n_sh):
+                        P.attention_partial(q, k, v, shards[s], w.block, w.causal, plans[s], o_p[s], m_p[s],
+                                            l_p[s], stream=stream)
+
+                t_part = _time_ms(partials, stream, flush, reps)
+                merge = lambda: dbsp.dbsp_merge_partials(o_p.view(n_sh, -1, w.d), m_p.view(n_sh, -1),
+                                                         l_p.view(n_sh, -1), out.view(-1, w.d), lse.view(-1),
+                                                         stream=stream)
+                t = _time_ms(merge, stream, flush, reps)
+                rows = w.B * w.H * w.S
+                nbytes = n_sh * rows * (4 * w.d + 8) + rows * (2 * w.d + 4)
+                line[f"merge_{layout}"] = {"us": 1e3 * t, "GB/s": nbytes / t / 1e6, "bytes": nbytes,
+                                           "frac_of_hbm": nbytes / t / 1e6 / float(peaks["hbm_gbs"]),
+                                           "partials_us": 1e3 * t_part,
+                                           "partials_TFLOP/s": flop / t_part / 1e9}
+        line["peaks"] = {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
+        status = dbsp.dbsp_device_status()
+        line["device_status"] = status
+        print(json.dumps(line), flush=True)
+        del q, k, v, out, lse, mask
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,11 +533,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dbsp", "reference"], default="dbsp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true", help="one line per workload, every kernel timed alone")
+    ap.add_argument("--workloads", default="", help="comma-separated workload names for --suite")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.suite:
+        return run_suite(args)
     return run_gpu(args)
 
 

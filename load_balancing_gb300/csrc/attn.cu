@@ -9,20 +9,22 @@
 //
 // Design (one persistent CTA per worker, 6 warps):
 //   warp 0      producer: scans the item's mask row with ballots, publishes the
-//               item (id, dense count) and issues TMA loads of the Q tile and of
+//               item (id, dense count) and issues TMA loads of the Q tile (two Q
+//               buffers, so the next item's Q lands during the current item) and of
 //               ONLY the dense K/V tiles into a ring of shared-memory stages, in
 //               the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
-//   warp 1      TMEM owner (512 columns); lane 0 issues tcgen05.mma:
-//               S = Q K^T into one of two TMEM S buffers, O += P V into the TMEM
-//               accumulator, each batch committed to an mbarrier.
+//   warp 1      TMEM owner (512 columns: S0 | S1 | O | P); lane 0 issues
+//               tcgen05.mma: S = Q K^T (both operands in shared memory) into one of
+//               two TMEM S buffers, and O += P V with P read from TMEM and V from
+//               shared memory (MN-major), each batch committed to an mbarrier.
 //   warps 2..5  softmax: thread = query row (TMEM lane). tcgen05.ld of the S row,
 //               diagonal masking, running max / sum in registers (base-2 units),
-//               P = exp2(S*scale*log2e - m) rounded to bf16 into shared memory in
-//               the 128-byte-swizzled K-major layout the MMA reads; the O
-//               accumulator is rescaled in TMEM only when a row's maximum grows by
-//               more than 2^8 (the result is exact either way: O and l always
-//               share one reference maximum). Then the epilogue (O / l, LSE or the
-//               partial triple with the true row maximum).
+//               P = exp2(S*scale*log2e - m) rounded to bf16 pairs and stored into
+//               the TMEM P columns with tcgen05.st; the O accumulator is rescaled in
+//               TMEM only when a row's maximum grows by more than 2^8 (the result is
+//               exact either way: O and l always share one reference maximum). Then
+//               the epilogue (O / l, LSE or the partial triple with the true row
+//               maximum).
 // Pipelining: S(j+1) is computed while the softmax of block j runs; PV(j) runs
 // while the softmax of block j+1 runs.
 //
@@ -44,9 +46,10 @@ namespace {
 
 using namespace dbsp::ptx;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 2 x 4 softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
+constexpr uint32_t kPCol = 384;  // P (bf16 pairs): the A operand of O += P V
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;    // 100 ms per teardown wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: P <= 256 between rescales
@@ -72,26 +75,29 @@ struct Cfg {
   static constexpr int kM = 128;                          // MMA rows (query tile)
   static constexpr int kChunk128 = 128 * 128;             // 128 rows x 128 B
   static constexpr int kQBytes = (D / 64) * kChunk128;
-  static constexpr int kPBytes = (BLOCK / 64) * kChunk128;
   static constexpr int kTileChunk = BLOCK * 128;          // BLOCK rows x 128 B
   static constexpr int kTileBytes = (D / 64) * kTileChunk;
   static constexpr int kTx = BLOCK * D * 2;               // bytes per Q / K / V tile load
   static constexpr int kBudget = 200 * 1024;
-  static constexpr int kStagesFit = (kBudget - kQBytes - kPBytes) / kTileBytes;
+  static constexpr int kQBufs = 2;                        // the next item's Q lands during this one
+  static constexpr int kStagesFit = (kBudget - kQBufs * kQBytes) / kTileBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kDataBytes = kQBytes + kPBytes + kStages * kTileBytes;
+  static constexpr int kDataBytes = kQBufs * kQBytes + kStages * kTileBytes;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kM, BLOCK, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kM, D, 0, 1);
   static_assert(kStages >= 2, "ring too small");
 };
 
 struct alignas(8) Ctrl {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t ring_full[8], ring_empty[8];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, pv_done;
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
+  uint64_t xbar[2], lbar[2];      // row-max (per block) and row-sum (per item) exchange
+  float xmax[2][2][128];          // [block parity][column half][row]
+  float xsum[2][2][128];          // [item parity][column half][row]
   int item_id[2], item_n[2], item_diag[2];
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -210,13 +216,15 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
     if (!ok || item < 0) break;
     if (n == 0) continue;
     if (lane == 0) {
-      ok = wait_bar(c, smem_u32(&c->q_empty), (q_cnt & 1) ^ 1, p.err);
+      const uint32_t qs = q_cnt % C::kQBufs, qu = q_cnt / C::kQBufs;
+      ok = wait_bar(c, smem_u32(&c->q_empty[qs]), (qu & 1) ^ 1, p.err);
       if (ok) {
-        const uint32_t full = smem_u32(&c->q_full);
+        const uint32_t full = smem_u32(&c->q_full[qs]);
         mbar_arrive_expect_tx(full, C::kTx);
         const int qrow = (int)(kv_row0 + (long long)(item % p.nQ) * BLOCK);
+        const uint32_t dst = smem_u32(sQ + qs * C::kQBytes);
 #pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(smem_u32(sQ + ch * C::kChunk128), tq, ch * 64, qrow, full);
+        for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kChunk128, tq, ch * 64, qrow, full);
       }
       ++q_cnt;
     }
@@ -252,20 +260,21 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
     const uint32_t issued = ring_cnt;
     for (uint32_t k = issued > (uint32_t)C::kStages ? issued - C::kStages : 0; k < issued; ++k)
       drain_bar(smem_u32(&c->ring_full[k % C::kStages]), (k / C::kStages) & 1);
-    if (q_cnt) drain_bar(smem_u32(&c->q_full), (q_cnt - 1) & 1);
+    for (uint32_t k = q_cnt > (uint32_t)C::kQBufs ? q_cnt - C::kQBufs : 0; k < q_cnt; ++k)
+      drain_bar(smem_u32(&c->q_full[k % C::kQBufs]), (k / C::kQBufs) & 1);
   }
   __syncwarp();
 }
 
 // ------------------------------------------------------------------ MMA issuer
 template <int BLOCK, int D>
-__device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sP, uint8_t* sRing,
+__device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sRing,
                         uint32_t tmem) {
   using C = Cfg<BLOCK, D>;
   uint32_t item_cnt = 0, q_cnt = 0, ring_cnt = 0, g = 0;
   long long blocks = 0;
   bool ok = true;
-  const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), ring_addr = smem_u32(sRing);
+  const uint32_t q_base = smem_u32(sQ), ring_addr = smem_u32(sRing);
   while (ok) {
     const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
     if (!wait_bar(c, smem_u32(&c->item_full[slot]), su & 1, p.err)) break;
@@ -274,8 +283,10 @@ __device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sP, 
     ++item_cnt;
     if (item < 0) break;
     if (n == 0) continue;
-    if (!wait_bar(c, smem_u32(&c->q_full), q_cnt & 1, p.err)) break;
+    const uint32_t qs = q_cnt % C::kQBufs;
+    if (!wait_bar(c, smem_u32(&c->q_full[qs]), (q_cnt / C::kQBufs) & 1, p.err)) break;
     ++q_cnt;
+    const uint32_t q_addr = q_base + qs * C::kQBytes;
     for (int jj = 0; jj <= n && ok; ++jj) {
       if (jj < n) {  // S(g + jj) = Q K^T
         const uint32_t gg = g + jj, sb = gg & 1;
@@ -293,7 +304,7 @@ __device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sP, 
         }
         mma_commit(smem_u32(&c->ring_empty[s]));
         mma_commit(smem_u32(&c->s_full[sb]));
-        if (jj == n - 1) mma_commit(smem_u32(&c->q_empty));
+        if (jj == n - 1) mma_commit(smem_u32(&c->q_empty[qs]));
         ++ring_cnt;
       }
       if (jj > 0) {  // O (+)= P V for block g + jj - 1
@@ -306,9 +317,8 @@ __device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sP, 
         const uint32_t vt = ring_addr + s * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < BLOCK / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(p_addr + (kk >> 2) * C::kChunk128 + (kk & 3) * 32, 16, 1024);
           const uint64_t b = smem_desc_sw128(vt + kk * 16 * 128, C::kTileChunk, 1024);
-          mma_bf16_ss(tmem + kOCol, a, b, C::kIdescPV, (jj > 1 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, b, C::kIdescPV, (jj > 1 || kk > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&c->ring_empty[s]));
         mma_commit(smem_u32(&c->pv_done));
@@ -325,15 +335,53 @@ __device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sP, 
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// (a0, a1) * (b, b) + (c, c) as one packed fp32x2 FMA
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Softmax warpgroups: warps 2..5 own columns [0, BLOCK/2) of every S row and columns
+// [0, D/2) of O; warps 6..9 own the other halves. Both halves of a row see the
+// same row maximum through a shared-memory exchange behind a bounded mbarrier, so
+// their rescale decisions agree; the row sum is combined once per item.
 template <int BLOCK, int D>
-__device__ void run_softmax(const AttnParams& p, Ctrl* c, uint8_t* sP, uint32_t tmem) {
+__device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
+  constexpr int CW = BLOCK / 2;  // S columns per thread
+  constexpr int DW = D / 2;      // O columns per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
+  const int half = (warp - 2) >> 2;
   const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
   const bool row_ok = r < BLOCK;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t s_off = half * CW, o_off = kOCol + half * DW, p_off = kPCol + half * (CW / 2);
   const bool partial = p.o_part != nullptr;
-  uint32_t item_cnt = 0, g = 0;
+  const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+  uint32_t item_cnt = 0, g = 0, items_done = 0;
   bool ok = true;
   while (ok) {
     const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
@@ -349,16 +397,15 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint8_t* sP, uint32_t 
     if (n == 0) {
       if (row_ok) {
         if (partial) {
-          float4* o = reinterpret_cast<float4*>(p.o_part + grow * D);
+          float4* o = reinterpret_cast<float4*>(p.o_part + grow * D + half * DW);
 #pragma unroll
-          for (int i = 0; i < D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          p.m_part[grow] = -INFINITY;
-          p.l_part[grow] = 0.f;
+          for (int i = 0; i < DW / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (half == 0) { p.m_part[grow] = -INFINITY; p.l_part[grow] = 0.f; }
         } else {
-          uint4* o = reinterpret_cast<uint4*>(p.out + grow * D);
+          uint4* o = reinterpret_cast<uint4*>(p.out + grow * D + half * DW);
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-          if (p.lse) p.lse[grow] = -INFINITY;
+          for (int i = 0; i < DW / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+          if (half == 0 && p.lse) p.lse[grow] = -INFINITY;
         }
       }
       continue;
@@ -368,100 +415,121 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint8_t* sP, uint32_t 
       const uint32_t sb = g & 1;
       if (!wait_bar(c, smem_u32(&c->s_full[sb]), (g >> 1) & 1, p.err)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[BLOCK];
-      if constexpr (BLOCK == 128) tmem_ld128_wait(lane_base + sb * 128, sr);
-      else tmem_ld64_wait(lane_base + sb * 128, sr);
+      uint32_t sr[CW];
+      if constexpr (CW == 64) tmem_ld64_wait(lane_base + sb * 128 + s_off, sr);
+      else tmem_ld32_wait(lane_base + sb * 128 + s_off, sr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->s_free[sb]));
 
+      float* s = reinterpret_cast<float*>(sr);
+      if (diag && jj == n - 1) {
+#pragma unroll
+        for (int k = 0; k < CW; ++k) if (s_off + k > (uint32_t)r) s[k] = -INFINITY;
+      }
+      // half-row maximum (3-input max, 4 independent chains)
+      static_assert(CW % 8 == 0, "half rows come in multiples of 8 columns");
+      float mxa[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mxa[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+      for (int k = 8; k < CW; k += 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mxa[i] = max3(mxa[i], s[k + 2 * i], s[k + 2 * i + 1]);
+      }
+      const float mh = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+      c->xmax[sb][half][r] = mh;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->xbar[sb]));
+      if (!wait_bar(c, smem_u32(&c->xbar[sb]), (g >> 1) & 1, p.err)) { ok = false; break; }
+      const float mx = fmaxf(mh, c->xmax[sb][half ^ 1][r]);
+
       float alpha = 1.f;
       bool rescale = false;
-      if (row_ok) {
-        float* s = reinterpret_cast<float*>(sr);
-        if (diag && jj == n - 1) {
+      const float mxs = mx * p.scale_log2;
+      m_true = fmaxf(m_true, mxs);
+      if (jj == 0) {
+        m_ref = mxs;
+      } else if (mxs > m_ref + kRescaleThreshold) {
+        alpha = ex2(m_ref - mxs);
+        l *= alpha;
+        m_ref = mxs;
+        rescale = true;
+      }
+      // P = exp2(s * scale_log2 - m_ref): packed fp32x2 FMA, MUFU ex2, packed sums
+      const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+      uint64_t acc[4] = {0, 0, 0, 0};
+      uint32_t pk[CW / 2];
 #pragma unroll
-          for (int k = 0; k < BLOCK; ++k) if (k > r) s[k] = -INFINITY;
-        }
-        float mx = s[0];
-#pragma unroll
-        for (int k = 1; k < BLOCK; ++k) mx = fmaxf(mx, s[k]);
-        const float mxs = mx * p.scale_log2;
-        m_true = fmaxf(m_true, mxs);
-        if (jj == 0) {
-          m_ref = mxs;
-        } else if (mxs > m_ref + kRescaleThreshold) {
-          alpha = ex2(m_ref - mxs);
-          l *= alpha;
-          m_ref = mxs;
-          rescale = true;
-        }
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < BLOCK; ++k) {
-          const float e = ex2(fmaf(s[k], p.scale_log2, -m_ref));
-          s[k] = e;
-          sum += e;
-        }
-        l += sum;
+      for (int k = 0; k < CW; k += 2) {
+        const uint64_t x = f2_fma(f2_pack(s[k], s[k + 1]), scale2, negm2);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        const float e0 = ex2(x0), e1 = ex2(x1);
+        acc[(k >> 1) & 3] = f2_add(acc[(k >> 1) & 3], f2_pack(e0, e1));
+        pk[k >> 1] = row_ok ? pack_bf16(e0, e1) : 0u;
+      }
+      {
+        const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        float t0, t1;
+        f2_unpack(t, t0, t1);
+        l += t0 + t1;
       }
       // P and O may be touched only once PV of the previous block is complete
       if (!wait_bar(c, smem_u32(&c->pv_done), (g & 1) ^ 1, p.err)) { ok = false; break; }
       tc_fence_after();
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < DW / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32_wait(lane_base + kOCol + cc * 32, o);
+          tmem_ld32_wait(lane_base + o_off + cc * 32, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_base + kOCol + cc * 32, o);
+          tmem_st32(lane_base + o_off + cc * 32, o);
         }
         tmem_wait_st();
       }
-      if (row_ok) {
-        const float* s = reinterpret_cast<const float*>(sr);
-        uint8_t* prow = sP + r * 128;
-#pragma unroll
-        for (int u = 0; u < BLOCK / 8; ++u) {
-          uint4 v;
-          v.x = pack_bf16(s[8 * u + 0], s[8 * u + 1]);
-          v.y = pack_bf16(s[8 * u + 2], s[8 * u + 3]);
-          v.z = pack_bf16(s[8 * u + 4], s[8 * u + 5]);
-          v.w = pack_bf16(s[8 * u + 6], s[8 * u + 7]);
-          const int chunk = u >> 3, unit = u & 7;
-          *reinterpret_cast<uint4*>(prow + chunk * Cfg<BLOCK, D>::kChunk128 + ((unit ^ (r & 7)) << 4)) = v;
-        }
-      }
-      fence_proxy_async_smem();
+      if constexpr (CW == 64) tmem_st32(lane_base + p_off, pk);
+      else tmem_st16(lane_base + p_off, pk);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c->p_full));
     }
     if (!ok) break;
+    // row sum of both halves (once per item)
+    const uint32_t lb = items_done & 1;
+    c->xsum[lb][half][r] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&c->lbar[lb]));
+    if (!wait_bar(c, smem_u32(&c->lbar[lb]), (items_done >> 1) & 1, p.err)) break;
+    l += c->xsum[lb][half ^ 1][r];
+    ++items_done;
     // epilogue: wait for the last PV of this item
     if (!wait_bar(c, smem_u32(&c->pv_done), (g - 1) & 1, p.err)) break;
     tc_fence_after();
-    uint32_t o[D];
-    if constexpr (D == 128) tmem_ld128_wait(lane_base + kOCol, o);
-    else tmem_ld64_wait(lane_base + kOCol, o);
+    uint32_t o[DW];
+    if constexpr (DW == 64) tmem_ld64_wait(lane_base + o_off, o);
+    else tmem_ld32_wait(lane_base + o_off, o);
     tc_fence_before();
     if (row_ok) {
       const float* of = reinterpret_cast<const float*>(o);
       constexpr float kLn2 = 0.693147180559945309f;
       if (partial) {
         const float f = ex2(m_ref - m_true);
-        float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D);
+        float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D + half * DW);
 #pragma unroll
-        for (int i = 0; i < D / 4; ++i)
+        for (int i = 0; i < DW / 4; ++i)
           dst[i] = make_float4(of[4 * i] * f, of[4 * i + 1] * f, of[4 * i + 2] * f, of[4 * i + 3] * f);
-        p.m_part[grow] = m_true * kLn2;
-        p.l_part[grow] = l * f;
+        if (half == 0) {
+          p.m_part[grow] = m_true * kLn2;
+          p.l_part[grow] = l * f;
+        }
       } else {
         const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * D);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * D + half * DW);
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
+        for (int i = 0; i < DW / 8; ++i) {
           uint4 v;
           v.x = pack_bf16(of[8 * i + 0] * inv, of[8 * i + 1] * inv);
           v.y = pack_bf16(of[8 * i + 2] * inv, of[8 * i + 3] * inv);
@@ -469,7 +537,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint8_t* sP, uint32_t 
           v.w = pack_bf16(of[8 * i + 6] * inv, of[8 * i + 7] * inv);
           dst[i] = v;
         }
-        if (p.lse) p.lse[grow] = (m_ref + __log2f(l)) * kLn2;
+        if (half == 0 && p.lse) p.lse[grow] = (m_ref + __log2f(l)) * kLn2;
       }
     }
   }
@@ -483,26 +551,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
-  uint8_t* sP = sQ + C::kQBytes;
-  uint8_t* sRing = sP + C::kPBytes;
+  uint8_t* sRing = sQ + C::kQBufs * C::kQBytes;
   Ctrl* c = reinterpret_cast<Ctrl*>(sRing + C::kStages * C::kTileBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t t_start = globaltimer();
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&c->q_full), 1);
-    mbar_init(smem_u32(&c->q_empty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c->q_full[b]), 1);
+      mbar_init(smem_u32(&c->q_empty[b]), 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&c->ring_full[s]), 1);
       mbar_init(smem_u32(&c->ring_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&c->s_full[b]), 1);
-      mbar_init(smem_u32(&c->s_free[b]), 4);
+      mbar_init(smem_u32(&c->s_free[b]), 8);
       mbar_init(smem_u32(&c->item_full[b]), 1);
-      mbar_init(smem_u32(&c->item_empty[b]), 5);
+      mbar_init(smem_u32(&c->item_empty[b]), 9);
+      mbar_init(smem_u32(&c->xbar[b]), 8);
+      mbar_init(smem_u32(&c->lbar[b]), 8);
     }
-    mbar_init(smem_u32(&c->p_full), 4);
+    mbar_init(smem_u32(&c->p_full), 8);
     mbar_init(smem_u32(&c->pv_done), 1);
     mbar_init(smem_u32(&c->drain), 1);
     c->abort_flag = 0;
@@ -526,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   if (warp == 0) {
     run_producer<BLOCK, D>(&tq, &tk, &tv, p, c, sQ, sRing, blockIdx.x);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<BLOCK, D>(p, c, sQ, sP, sRing, tmem);
+    if (lane == 0) run_mma<BLOCK, D>(p, c, sQ, sRing, tmem);
     __syncwarp();
   } else {
-    run_softmax<BLOCK, D>(p, c, sP, tmem);
+    run_softmax<BLOCK, D>(p, c, tmem);
   }
 
   tc_fence_before();

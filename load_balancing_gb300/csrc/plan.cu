@@ -7,19 +7,30 @@
 // id, ties between workers go to the lowest index, the bonus enters only the
 // choice and the worker accrues the item's true load.
 //
-// One CTA of 256 threads:
-//   phase 0  check loads/home, find the load range;
-//   phase 1  stable order by (load desc, id asc): a counting sort through a
-//            shared-memory histogram (loads <= 32767), else rank-by-comparison
-//            (n <= 16384). The order is written into `worklist`;
-//   phase 2  the greedy, one warp: every lane keeps the loads of workers
-//            lane, lane+32, ... in registers as packed keys (load << 11 | worker),
-//            so (load, worker) order is plain int64 order; the warp minimum is two
-//            redux.sync reductions (high word, then low word among the tied);
-//            `worker_of[i]` temporarily holds worker + m * (rank within worker);
+// Worker keys are packed as (load << 11 | worker), so the greedy's choice (lowest
+// load, then lowest index) is the smallest int64 key. One CTA of 256 threads:
+//
+//   phase 0  check loads and home, find the load range; when n <= 45056 and every
+//            load <= 4095 the loads are staged in shared memory as uint16
+//            ("staged" path), otherwise the kernel works from global memory;
+//   phase 1  the stable order (load desc, id asc): a counting sort through a
+//            shared-memory histogram, its stable scatter done by one warp with
+//            match_any (or rank-by-comparison for n <= 16384 with large loads);
+//   phase 2  the greedy, one warp.
+//            Without a bonus it goes one RUN of equal loads w at a time, in
+//            batches: with the workers' keys sorted ascending in A, every key
+//            below A[0] + (w << 11) is taken in order by the next items of the
+//            run -- each re-keyed worker (key + (w << 11)) is above all of
+//            them, so the one-at-a-time greedy picks exactly this sequence --
+//            then the re-keyed batch is merged back into A (binary searches).
+//            With a bonus the key of item i's home worker is lowered by the
+//            bonus for that choice only, so items go one at a time: every lane
+//            keeps the keys of workers lane, lane+32, ... in registers and the
+//            warp minimum takes two redux.sync (high word, then low word).
+//            worker_of[i] temporarily holds worker + m * (rank within worker);
 //   phase 3  CSR offsets by a block scan of the per-worker counts, then the
 //            scatter of every item to offsets[worker] + rank.
-// The output arrays are the only global working storage.
+// Global working storage is the output arrays only.
 #include <algorithm>
 #include <climits>
 
@@ -28,18 +39,25 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kStagedMaxItems = 45056;
+constexpr int kStagedMaxLoad = 2047;
 constexpr int kMaxLoadCounting = 32767;
 constexpr int kMaxItemsCompare = 16384;
 constexpr int kWorkerBits = 11;  // worker index < 2048 in the packed key
+constexpr long long kWorkerMask = (1LL << kWorkerBits) - 1;
 constexpr long long kKeyNone = LLONG_MAX;
+
+constexpr size_t kStagedBytes = 2ull * kStagedMaxItems + 4ull * (kStagedMaxLoad + 2) + 4ull * 8 * (kStagedMaxLoad + 1);
+constexpr size_t kGlobalBytes = 4ull * (kMaxLoadCounting + 2 > kMaxItemsCompare ? kMaxLoadCounting + 2 : kMaxItemsCompare);
+constexpr size_t kDynBytes = kStagedBytes > kGlobalBytes ? kStagedBytes : kGlobalBytes;
 
 struct PlanShared {
   int min_load, max_load, bad_home;
   int scan[kThreads / 32 + 1];
 };
 
-// Exclusive scan over `n` ints in shared memory `a` (in place). Returns the total.
-__device__ int block_exclusive_scan(int* a, int n, int* warp_sums) {
+// Exclusive scan over `n` ints in shared memory `a` (in place). All threads call it.
+__device__ void block_exclusive_scan(int* a, int n, int* warp_sums) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (n + kThreads - 1) / kThreads;
   const int lo = min(n, tid * per), hi = min(n, lo + per);
@@ -56,14 +74,21 @@ __device__ int block_exclusive_scan(int* a, int n, int* warp_sums) {
   if (tid == 0) {
     int run = 0;
     for (int w = 0; w < kThreads / 32; ++w) { const int t = warp_sums[w]; warp_sums[w] = run; run += t; }
-    warp_sums[kThreads / 32] = run;
   }
   __syncthreads();
   int run = warp_sums[warp] + x - s;
   for (int j = lo; j < hi; ++j) { const int t = a[j]; a[j] = run; run += t; }
-  const int total = warp_sums[kThreads / 32];
   __syncthreads();
-  return total;
+}
+
+// Number of keys < v in the ascending range a[lo, hi).
+__device__ __forceinline__ int count_below(const long long* a, int lo, int hi, long long v) {
+  int l = lo, h = hi;
+  while (l < h) {
+    const int mid = (l + h) >> 1;
+    if (a[mid] < v) l = mid + 1; else h = mid;
+  }
+  return l - lo;
 }
 
 template <int KMAX>
@@ -74,15 +99,230 @@ __device__ __forceinline__ long long lane_minimum(const long long (&key)[KMAX]) 
   return m;
 }
 
+struct Sorted {  // the stable order, staged in shared memory or in the worklist
+  const uint16_t* smem;
+  const int32_t* gmem;
+  __device__ __forceinline__ int operator[](int t) const { return smem ? (int)smem[t] : gmem[t]; }
+};
+
+// One merge of a batch (see greedy_batched): E = bp + tail keys are re-placed, KE per
+// lane, as straight-line code so that the KE binary searches of a lane interleave.
+template <int KE>
+__device__ __forceinline__ void merge_step(long long* A, int m, int h, int b, int bp, int E, long long step,
+                                           int iters, int h_new) {
+  const int lane = threadIdx.x & 31;
+  long long val[KE], tgt[KE];
+  int lo[KE], hi[KE];
+#pragma unroll
+  for (int t = 0; t < KE; ++t) {
+    const int k = lane + 32 * t;
+    const bool live = k < E;
+    const bool is_y = k < bp;
+    int src = is_y ? k : b + k - bp;
+    src = live ? src : 0;
+    int x = h + src;
+    x = x >= m ? x - m : x;
+    const long long a = A[x];
+    val[t] = is_y ? a + step : a;
+    tgt[t] = is_y ? val[t] : a - step;
+    lo[t] = !live ? 0 : (is_y ? b : 0);
+    hi[t] = !live ? 0 : (is_y ? m : bp);
+  }
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int t = 0; t < KE; ++t) {
+      const int mid = (lo[t] + hi[t]) >> 1;  // lo == hi <= m still indexes the list
+      int x = h + mid;
+      x = x >= m ? x - m : x;
+      x = x >= m ? x - m : x;
+      const long long am = A[x];
+      const bool go = lo[t] < hi[t];
+      const bool less = am < tgt[t];
+      lo[t] = go && less ? mid + 1 : lo[t];
+      hi[t] = go && !less ? mid : hi[t];
+    }
+  }
+  int dst[KE];
+#pragma unroll
+  for (int t = 0; t < KE; ++t) {
+    const int k = lane + 32 * t;
+    const int pos = k < bp ? (b - bp) + k + (lo[t] - b) : (b - bp) + (k - bp) + lo[t];
+    int x = h_new + pos;
+    x = x >= m ? x - m : x;
+    dst[t] = k < E ? x : -1;
+  }
+  __syncwarp();  // all reads of the old order are done
+#pragma unroll
+  for (int t = 0; t < KE; ++t)
+    if (dst[t] >= 0) A[dst[t]] = val[t];
+  __syncwarp();
+}
+
+// Phase 2 without a bonus: batches per run of equal loads (one warp), KMAX keys per lane.
+// The worker keys stay sorted in a circular list: logical key i is A[(h + i) mod m].
+// One batch of a run with load w (wk = w << 11), b = number of keys below
+// A[h] + wk:
+//   * b > 1: the next bp = min(b, r) items take the first bp keys in order (each
+//     re-keyed key is at or above the threshold, above every key still in the
+//     batch), so the one-at-a-time greedy makes exactly these picks;
+//   * b == 1: the minimum keeps winning while its key stays below the runner-up,
+//     for q = ceil((key1 - key0) / wk) picks, and is re-keyed once by q * wk.
+// Then the head advances past the picked keys; the keys below the threshold do not
+// move, and only the "tail" (keys at or above the threshold) is merged with the
+// re-keyed keys, each placed by a binary search in the other list.
+template <int KMAX>
+__device__ __forceinline__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbins, int max_load, int n, int m,
+                               long long* A, int* counts, long long* final_load,
+                               int32_t* __restrict__ worker_of) {
+  const int lane = threadIdx.x & 31;
+  for (int j = lane; j < m; j += 32) { A[j] = j; counts[j] = 0; }
+  __syncwarp();
+  int h = 0;
+  auto phys = [&](int i) { const int x = h + i; return x >= m ? x - m : x; };
+  int s = 0;
+  for (int bin = 0; bin < nbins && s < n; ++bin) {
+    const int e = bin_end[bin];
+    int r = e - s;
+    if (r <= 0) continue;
+    const int w = max_load - bin;
+    if (w == 0) {  // zero loads never change a key: they all go to the current minimum
+      const int p0 = (int)(A[h] & kWorkerMask);
+      const int base = counts[p0];
+      for (int j = lane; j < r; j += 32) worker_of[sorted[s + j]] = p0 + m * (base + j);
+      __syncwarp();
+      if (lane == 0) counts[p0] = base + r;
+      __syncwarp();
+      s = e;
+      continue;
+    }
+    const long long wk = (long long)w << kWorkerBits;
+    while (r > 0) {
+      const long long key0 = A[h];
+      const long long thr = key0 + wk;
+      int c = 0;
+#pragma unroll
+      for (int t = 0; t < KMAX; ++t) {  // order does not matter for a count
+        const int j = lane + 32 * t;
+        c += (j < m) && A[j < m ? j : 0] < thr;
+      }
+      const int b = __reduce_add_sync(0xffffffffu, c);
+      int bp, picks;
+      long long step;  // amount added to each picked key
+      if (b == 1) {
+        picks = m > 1 ? (int)min((long long)r, (A[phys(1)] - key0 + wk - 1) / wk) : r;
+        bp = 1;
+        step = (long long)picks * wk;
+        const int p = (int)(key0 & kWorkerMask);
+        const int base = counts[p];
+        for (int j = lane; j < picks; j += 32) worker_of[sorted[s + j]] = p + m * (base + j);
+        __syncwarp();
+        if (lane == 0) counts[p] = base + picks;
+      } else {
+        bp = min(b, r);
+        picks = bp;
+        step = wk;
+        for (int j = lane; j < bp; j += 32) {
+          const int p = (int)(A[phys(j)] & kWorkerMask);
+          const int rank = counts[p];
+          counts[p] = rank + 1;
+          worker_of[sorted[s + j]] = p + m * rank;
+        }
+      }
+      // merge region: new logical positions [b - bp, m) after the head moves by bp;
+      // element k < bp is the re-keyed key Y_k = key(k) + step, element k >= bp the
+      // tail key at logical b + (k - bp)
+      const int tail = m - b;
+      const int E = bp + tail;
+      const int iters = 32 - __clz(max(bp, tail));  // enough halvings for the larger list
+      const int h_new = phys(bp);
+      if (E <= 32) merge_step<1>(A, m, h, b, bp, E, step, iters, h_new);
+      else if (E <= 64 || KMAX <= 2) merge_step<(KMAX < 2 ? KMAX : 2)>(A, m, h, b, bp, E, step, iters, h_new);
+      else if (E <= 128 || KMAX <= 4) merge_step<(KMAX < 4 ? KMAX : 4)>(A, m, h, b, bp, E, step, iters, h_new);
+      else if (E <= 256 || KMAX <= 8) merge_step<(KMAX < 8 ? KMAX : 8)>(A, m, h, b, bp, E, step, iters, h_new);
+      else if (E <= 512 || KMAX <= 16) merge_step<(KMAX < 16 ? KMAX : 16)>(A, m, h, b, bp, E, step, iters, h_new);
+      else merge_step<KMAX>(A, m, h, b, bp, E, step, iters, h_new);
+      h = h_new;
+      s += picks;
+      r -= picks;
+    }
+  }
+  for (int j = lane; j < m; j += 32) final_load[A[j] & kWorkerMask] = A[j] >> kWorkerBits;
+}
+
+// Phase 2 with a bonus (or without staged runs): one item at a time (one warp).
+template <int KMAX>
+__device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t* __restrict__ loads,
+                              const int32_t* __restrict__ home, int bonus, int n, int m, int* counts,
+                              long long* final_load, int32_t* __restrict__ worker_of) {
+  const int lane = threadIdx.x & 31;
+  long long key[KMAX];
+  int cnt[KMAX];
+#pragma unroll
+  for (int q = 0; q < KMAX; ++q) {
+    const int p = lane + 32 * q;
+    key[q] = p < m ? (long long)p : kKeyNone;  // load 0, worker p
+    cnt[q] = 0;
+  }
+  long long my_min = lane_minimum(key);
+  const long long bonus_key = (long long)bonus << kWorkerBits;
+  for (int base = 0; base < n; base += 32) {
+    const int t = base + lane;
+    int my_i = 0, my_w = 0, my_h = -1;
+    if (t < n) {
+      my_i = sorted[t];
+      my_w = loads[my_i];
+      if (home) my_h = home[my_i];
+    }
+    const int chunk = min(32, n - base);
+    for (int s = 0; s < chunk; ++s) {
+      const int i = __shfl_sync(0xffffffffu, my_i, s);
+      const int w = __shfl_sync(0xffffffffu, my_w, s);
+      const int h = __shfl_sync(0xffffffffu, my_h, s);
+      long long cand = my_min;
+      if (h >= 0 && (h & 31) == lane) {
+        long long kh = kKeyNone;
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) kh = q == (h >> 5) ? key[q] : kh;
+        kh -= bonus_key;
+        cand = kh < cand ? kh : cand;
+      }
+      const int hi = (int)(cand >> 32);
+      const int min_hi = __reduce_min_sync(0xffffffffu, hi);
+      const unsigned lo = hi == min_hi ? (unsigned)(cand & 0xffffffffu) : 0xffffffffu;
+      const unsigned min_lo = __reduce_min_sync(0xffffffffu, lo);
+      const int p = (int)(min_lo & (unsigned)kWorkerMask);
+      if ((p & 31) == lane) {
+        const int qp = p >> 5;
+        int rank = 0;
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) {
+          const bool me = q == qp;
+          rank = me ? cnt[q] : rank;
+          cnt[q] += me;
+          key[q] += me ? ((long long)w << kWorkerBits) : 0;
+        }
+        worker_of[i] = p + m * rank;
+        my_min = lane_minimum(key);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < KMAX; ++q) {
+    const int p = lane + 32 * q;
+    if (p < m) { counts[p] = cnt[q]; final_load[p] = key[q] >> kWorkerBits; }
+  }
+}
+
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     const int32_t* __restrict__ loads, const int32_t* __restrict__ home, int n, int m,
     int bonus, int32_t* __restrict__ worker_of, int32_t* __restrict__ offsets,
     int32_t* __restrict__ worklist, int64_t* __restrict__ worker_loads, int* err) {
-  extern __shared__ int dyn[];  // histogram / cursor, or a copy of the loads
+  extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ PlanShared sh;
   __shared__ int counts[DBSP_MAX_WORKERS + 1];
   __shared__ long long final_load[DBSP_MAX_WORKERS];
+  __shared__ long long keys[2][DBSP_MAX_WORKERS];
   const int tid = threadIdx.x, lane = tid & 31;
 
   // ---- phase 0: validate and find the load range
@@ -99,40 +339,88 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   if (badh) atomicOr(&sh.bad_home, 1);
   __syncthreads();
   const bool ok_vals = n == 0 || (sh.min_load >= 0 && !sh.bad_home);
-  const bool counting = n == 0 || sh.max_load <= kMaxLoadCounting;
+  const int max_load = n ? sh.max_load : 0;
+  const bool staged = n <= kStagedMaxItems && max_load <= kStagedMaxLoad;
+  const bool counting = max_load <= kMaxLoadCounting;
   if (!ok_vals || (!counting && n > kMaxItemsCompare)) {
     if (tid == 0) dbsp::report(err, ok_vals ? DBSP_ERR_UNSUPPORTED : DBSP_ERR_INVALID_ARG);
     for (int p = tid; p <= m; p += kThreads) offsets[p] = 0;
     return;
   }
-  const int max_load = n ? sh.max_load : 0;
+  const int nbins = max_load + 1;
 
-  // ---- phase 1: stable order by (load desc, id asc) into worklist
-  if (counting) {
-    int* cursor = dyn;  // bins are indexed by (max_load - load): descending loads first
-    const int nbins = max_load + 1;
-    for (int b = tid; b < nbins; b += kThreads) cursor[b] = 0;
+  // ---- phase 1: stable order by (load desc, id asc)
+  Sorted sorted{nullptr, worklist};
+  const int* bin_end = nullptr;  // bin_end[b] = one past the last sorted position of bin b
+  if (staged) {
+    // 8 warps each take a contiguous id segment: per-warp histograms, a scan over
+    // (bin, warp), then each warp scatters its segment in id order (stable)
+    const int n_pad = (n + 7) & ~7;
+    uint16_t* order = reinterpret_cast<uint16_t*>(dyn);
+    int* cursor = reinterpret_cast<int*>(order + n_pad);  // [nbins + 1]
+    int* whist = cursor + (nbins + 1);                    // [8][nbins]
+    const int warp = tid >> 5;
+    constexpr int kWarps = kThreads / 32;
+    const int seg = (n + kWarps - 1) / kWarps;
+    const int lo = min(n, warp * seg), hi = min(n, lo + seg);
+    for (int b = tid; b < kWarps * nbins; b += kThreads) whist[b] = 0;
+    __syncthreads();
+    for (int i = lo + lane; i < hi; i += 32) atomicAdd(&whist[warp * nbins + (max_load - loads[i])], 1);
+    __syncthreads();
+    for (int b = tid; b <= nbins; b += kThreads) {
+      int t = 0;
+      if (b < nbins)
+        for (int w = 0; w < kWarps; ++w) t += whist[w * nbins + b];
+      cursor[b] = t;
+    }
+    __syncthreads();
+    block_exclusive_scan(cursor, nbins + 1, sh.scan);
+    for (int b = tid; b < nbins; b += kThreads) {
+      int run = cursor[b];
+      for (int w = 0; w < kWarps; ++w) { const int t = whist[w * nbins + b]; whist[w * nbins + b] = run; run += t; }
+    }
+    __syncthreads();
+    int* mine = whist + warp * nbins;
+    for (int base = lo; base < hi; base += 32) {
+      const int i = base + lane;
+      const unsigned active = __ballot_sync(0xffffffffu, i < hi);
+      if (i < hi) {
+        const int bin = max_load - loads[i];
+        const unsigned peers = __match_any_sync(active, bin);
+        const unsigned below = peers & ((1u << lane) - 1);
+        order[mine[bin] + __popc(below)] = (uint16_t)i;
+        __syncwarp(active);
+        if (below == 0) mine[bin] += __popc(peers);
+      }
+      __syncwarp();
+    }
+    sorted = Sorted{order, nullptr};
+    bin_end = cursor + 1;
+  } else if (counting) {
+    int* cursor = reinterpret_cast<int*>(dyn);
+    for (int b = tid; b <= nbins; b += kThreads) cursor[b] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) atomicAdd(&cursor[max_load - loads[i]], 1);
     __syncthreads();
-    block_exclusive_scan(cursor, nbins, sh.scan);
-    if (tid < 32) {  // stable scatter in id order, 32 ids at a time
+    block_exclusive_scan(cursor, nbins + 1, sh.scan);
+    if (tid < 32) {  // stable scatter in id order, 32 ids at a time, into the worklist
       for (int base = 0; base < n; base += 32) {
         const int i = base + lane;
         const unsigned active = __ballot_sync(0xffffffffu, i < n);
         if (i < n) {
           const int bin = max_load - loads[i];
           const unsigned peers = __match_any_sync(active, bin);
-          const int pos = cursor[bin] + __popc(peers & ((1u << lane) - 1));
-          worklist[pos] = i;
+          const unsigned below = peers & ((1u << lane) - 1);
+          worklist[cursor[bin] + __popc(below)] = i;
           __syncwarp(active);
-          if ((peers & ((1u << lane) - 1)) == 0) cursor[bin] += __popc(peers);
+          if (below == 0) cursor[bin] += __popc(peers);
         }
         __syncwarp();
       }
     }
+    bin_end = cursor;  // after the scatter each cursor is the end of its bin
   } else {
-    int* w_s = dyn;
+    int* w_s = reinterpret_cast<int*>(dyn);
     for (int i = tid; i < n; i += kThreads) w_s[i] = loads[i];
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) {
@@ -149,59 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
 
   // ---- phase 2: the greedy (warp 0)
   if (tid < 32) {
-    long long key[KMAX];
-    int cnt[KMAX];
-#pragma unroll
-    for (int q = 0; q < KMAX; ++q) {
-      const int p = lane + 32 * q;
-      key[q] = p < m ? (long long)p : kKeyNone;  // load 0, worker p
-      cnt[q] = 0;
-    }
-    long long my_min = lane_minimum(key);
-    const long long bonus_key = (long long)bonus << kWorkerBits;
-    for (int base = 0; base < n; base += 32) {
-      const int t = base + lane;
-      int my_i = 0, my_w = 0, my_h = -1;
-      if (t < n) {
-        my_i = worklist[t];
-        my_w = loads[my_i];
-        if (home) my_h = home[my_i];
-      }
-      const int chunk = min(32, n - base);
-      for (int s = 0; s < chunk; ++s) {
-        const int i = __shfl_sync(0xffffffffu, my_i, s);
-        const int w = __shfl_sync(0xffffffffu, my_w, s);
-        const int h = __shfl_sync(0xffffffffu, my_h, s);
-        long long cand = my_min;
-        if (h >= 0 && (h & 31) == lane) {
-          long long kh = kKeyNone;
-#pragma unroll
-          for (int q = 0; q < KMAX; ++q) if (q == (h >> 5)) kh = key[q];
-          kh -= bonus_key;
-          cand = kh < cand ? kh : cand;
-        }
-        const int hi = (int)(cand >> 32);
-        const int min_hi = __reduce_min_sync(0xffffffffu, hi);
-        const unsigned lo = hi == min_hi ? (unsigned)(cand & 0xffffffffu) : 0xffffffffu;
-        const unsigned min_lo = __reduce_min_sync(0xffffffffu, lo);
-        const int p = (int)(min_lo & ((1u << kWorkerBits) - 1));
-        if ((p & 31) == lane) {
-          const int qp = p >> 5;
-          int rank = 0;
-#pragma unroll
-          for (int q = 0; q < KMAX; ++q) {
-            if (q == qp) { key[q] += (long long)w << kWorkerBits; rank = cnt[q]; cnt[q] += 1; }
-          }
-          worker_of[i] = p + m * rank;
-          my_min = lane_minimum(key);
-        }
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < KMAX; ++q) {
-      const int p = lane + 32 * q;
-      if (p < m) { counts[p] = cnt[q]; final_load[p] = key[q] >> kWorkerBits; }
-    }
+    if (counting && (home == nullptr || bonus == 0))
+      greedy_batched<KMAX>(sorted, bin_end, nbins, max_load, n, m, keys[0], counts, final_load, worker_of);
+    else
+      greedy_serial<KMAX>(sorted, loads, home, bonus, n, m, counts, final_load, worker_of);
   }
   __syncthreads();
 
@@ -223,12 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
 template <int KMAX>
 int launch(const int32_t* loads, const int32_t* home, int n, int m, int bonus, int32_t* worker_of,
            int32_t* offsets, int32_t* worklist, int64_t* worker_loads, int* err, cudaStream_t s) {
-  const size_t smem = sizeof(int) * (size_t)std::max(kMaxLoadCounting + 1, kMaxItemsCompare);
   auto kernel = lpt_plan_kernel<KMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(lpt_plan)");
-  kernel<<<1, kThreads, smem, s>>>(loads, home, n, m, bonus, worker_of, offsets, worklist,
-                                   worker_loads, err);
+  kernel<<<1, kThreads, kDynBytes, s>>>(loads, home, n, m, bonus, worker_of, offsets, worklist, worker_loads,
+                                        err);
   DBSP_LAUNCH_CHECK("launch lpt_plan");
   return DBSP_OK;
 }

@@ -80,6 +80,24 @@ def test_large_loads_take_comparison_sort(built_library, cuda_device):
     _assert_same(_plan(loads, 37), OP.lpt_plan(loads, 37))
 
 
+@pytest.mark.parametrize("n,hi,m", [(50000, 100, 148), (3000, 20000, 64), (2000, 4097, 1000)])
+def test_unstaged_counting_paths(built_library, cuda_device, n, hi, m):
+    """Beyond the shared-memory staging limits (n > 45056 or a load > 4095) the kernel
+    sorts through global memory; the result must not change."""
+    rng = np.random.default_rng(n + hi)
+    loads = rng.integers(0, hi, n)
+    loads[0] = hi - 1
+    _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+
+
+def test_zero_loads_and_single_worker(built_library, cuda_device):
+    rng = np.random.default_rng(12)
+    loads = rng.integers(0, 3, 5000)  # long runs of 0, 1, 2
+    for m in (1, 2, 5, 148):
+        _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+    _assert_same(_plan(np.zeros(100, dtype=np.int64), 7), OP.lpt_plan(np.zeros(100, dtype=np.int64), 7))
+
+
 def test_more_workers_than_items(built_library, cuda_device):
     loads = [5, 9, 9, 1, 0, 3]
     _assert_same(_plan(loads, 10), OP.lpt_plan(loads, 10))
