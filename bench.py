@@ -35,6 +35,21 @@ METRIC = "block-sparse attn fwd TFLOP/s on dense blocks, % of bf16 TC peak, SM s
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes (read + write) of one attention launch on this workload, from the ncu capture
+# summarised in profiles/attn_fwd_llm.md, valid only for the kernel source it was taken on.
+NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "587dfdda083c9c10", "bytes": 310.2e6,
+                    "source": "profiles/attn_fwd_llm.md"}
+
+
+def attn_traffic():
+    """Profiled bytes per launch, or None when attn.cu changed since the capture."""
+    import hashlib
+
+    path = os.path.join(ROOT, "load_balancing_gb300", "csrc", "attn.cu")
+    with open(path, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return NCU_ATTN_TRAFFIC["bytes"] if sha.startswith(NCU_ATTN_TRAFFIC["attn_sha256_prefix"]) else None
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -387,7 +402,8 @@ def run_gpu(args):
         "loads_plus_plan_us": 1e3 * statistics.mean(plan_ms),
         "attn_us": 1e6 * attn_avg_s,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": attn_tflops / peak, "traffic": None,
+                     "frac": attn_tflops / peak, "traffic": attn_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "peak_source": f"{peak_src} bf16 dense (burst, cuBLAS)",
                      "kernel": "attn_fwd_kernel<128,128>"},
         "e2e": {"value": total_flop / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -127,6 +127,8 @@ DBSP_API int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_item
  *               no admissible key get O = 0 and lse = -inf.
  * Partial mode (out == NULL; o_part, m_part, l_part all non-NULL; lse ignored):
  *   o_part      fp32 [B, H, S, d]: unnormalised O relative to the row maximum.
+ *               Rows of items with no dense block are left unwritten: their
+ *               (m, l) = (-inf, 0) marks them empty and no reader looks at them.
  *   m_part      fp32 [B, H, S]: row maximum of the scaled scores (-inf if empty).
  *   l_part      fp32 [B, H, S]: row sum of exp(score - m) (0 if empty).
  * cta_timing    int64 [n_workers * 3] or NULL: per worker the %globaltimer (ns)

@@ -7,24 +7,29 @@
 // partial (O, m, l) of one KV shard. Causal (6D attention notes §2.3): blocks
 // above the diagonal are skipped and the diagonal block is masked per element.
 //
-// Design (one persistent CTA per worker, 6 warps):
-//   warp 0      producer: scans the item's mask row with ballots, publishes the
-//               item (id, dense count) and issues TMA loads of the Q tile (two Q
-//               buffers, so the next item's Q lands during the current item) and of
-//               ONLY the dense K/V tiles into a ring of shared-memory stages, in
-//               the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
+// Design (one persistent CTA per worker, 10 warps):
+//   warp 0      producer: reads the item's mask row 16 bytes per lane (the next
+//               item's first 512 columns are fetched while the current item's tiles
+//               are issued), publishes the item (id, dense count) and issues TMA
+//               loads of the Q tile (two Q buffers, so the next item's Q lands during
+//               the current item) and of ONLY the dense K/V tiles into a ring of
+//               shared-memory stages, in the order the MMA warp consumes them:
+//               K0, K1, V0, K2, V1, ...
 //   warp 1      TMEM owner (512 columns: S0 | S1 | O | P); lane 0 issues
 //               tcgen05.mma: S = Q K^T (both operands in shared memory) into one of
 //               two TMEM S buffers, and O += P V with P read from TMEM and V from
 //               shared memory (MN-major), each batch committed to an mbarrier.
-//   warps 2..5  softmax: thread = query row (TMEM lane). tcgen05.ld of the S row,
-//               diagonal masking, running max / sum in registers (base-2 units),
-//               P = exp2(S*scale*log2e - m) rounded to bf16 pairs and stored into
-//               the TMEM P columns with tcgen05.st; the O accumulator is rescaled in
-//               TMEM only when a row's maximum grows by more than 2^8 (the result is
-//               exact either way: O and l always share one reference maximum). Then
-//               the epilogue (O / l, LSE or the partial triple with the true row
-//               maximum).
+//   warps 2..9  softmax, two warpgroups: thread = query row (TMEM lane); warps 2..5
+//               own the left half of the S columns and of the O columns, warps 6..9
+//               the right halves. tcgen05.ld of the half row, diagonal masking, the
+//               half-row maxima are exchanged through shared memory so both halves
+//               share one running maximum (base-2 units); P = exp2(S*scale*log2e - m)
+//               rounded to bf16 pairs and stored into the TMEM P columns with
+//               tcgen05.st; the O accumulator is rescaled in TMEM only when a row's
+//               maximum grows by more than 2^8 (the result is exact either way: O and
+//               l always share one reference maximum). Then the epilogue (O / l, LSE,
+//               or the partial triple with the true row maximum; an empty partial
+//               writes only m = -inf, l = 0).
 // Pipelining: S(j+1) is computed while the softmax of block j runs; PV(j) runs
 // while the softmax of block j+1 runs.
 //
@@ -99,6 +104,7 @@ struct alignas(8) Ctrl {
   float xmax[2][2][128];          // [block parity][column half][row]
   float xsum[2][2][128];          // [item parity][column half][row]
   int item_id[2], item_n[2], item_diag[2];
+  alignas(4) uint16_t scan_bits[32];  // producer: dense bits of one 512-column mask chunk
   uint32_t tmem_base;
   volatile int abort_flag;
   long long blocks_done;
@@ -147,16 +153,72 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // ------------------------------------------------------------------ producer
+// 4-bit mask of the non-zero bytes of x (bit i <-> byte i).
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
+  const uint32_t t = __vcmpne4(x, 0u) & 0x01010101u;
+  return (t * 0x01020408u) >> 24;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+  return v;
+}
+
+// The mask row of an item is read 512 columns at a time: lane l holds the 16 bytes
+// of columns [c0 + 16 l, c0 + 16 l + 16). Rows are read with one 16-byte load per
+// lane when every row starts on a 16-byte boundary, else byte by byte.
+struct RowScan {
+  const uint8_t* mask;
+  int nK, nQ, causal, n_items;
+  bool vec;
+  int lane;
+
+  __device__ int limit(int item) const {
+    return causal ? min(nK, item % nQ + 1) : nK;
+  }
+  // raw bytes of the lane's 16 columns of chunk c0 (zero where col >= limit)
+  __device__ uint4 load(int item, int c0) const {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (item < 0 || item >= n_items) return v;
+    const int lim = limit(item), col = c0 + 16 * lane;
+    if (col >= lim) return v;
+    const uint8_t* row = mask + (long long)item * nK;
+    if (vec) return ld_nc_v4(row + col);  // col + 16 <= nK: nK is a multiple of 16
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int t = 0; t < 16 && col + t < lim; ++t) w[t >> 2] |= (uint32_t)row[col + t] << (8 * (t & 3));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  // dense-block bits of those columns, limited to col < lim
+  __device__ uint32_t bits(uint4 v, int c0, int lim) const {
+    const int rem = lim - (c0 + 16 * lane);
+    if (rem <= 0) return 0u;
+    uint32_t b = nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4) | (nonzero_bytes(v.z) << 8) |
+                 (nonzero_bytes(v.w) << 12);
+    return rem < 16 ? b & ((1u << rem) - 1u) : b;
+  }
+};
+
 template <int BLOCK, int D>
 __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sRing, int worker) {
   using C = Cfg<BLOCK, D>;
+  constexpr unsigned kAll = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   int begin = p.offsets[worker], end = p.offsets[worker + 1];
   if (begin < 0 || end < begin) {
     if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
     begin = end = 0;
   }
+  RowScan rs;
+  rs.mask = p.mask;
+  rs.nK = p.nK;
+  rs.nQ = p.nQ;
+  rs.causal = p.causal;
+  rs.n_items = p.n_items;
+  rs.vec = ((reinterpret_cast<uintptr_t>(p.mask) | (uintptr_t)p.nK) & 15u) == 0;
+  rs.lane = lane;
   uint32_t item_cnt = 0, q_cnt = 0, ring_cnt = 0;
   bool ok = true;
   // q/k/v tile issue (lane 0 only)
@@ -171,34 +233,35 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
     ++ring_cnt;
     return true;
   };
+  auto item_at = [&](int idx) -> int { return idx < end ? __ldg(p.worklist + idx) : -1; };
 
+  // Item ids run two entries ahead and the first mask chunk one item ahead, so their
+  // load latency hides under the previous item's tile issue.
+  int item_next = item_at(begin);
+  int item_after = item_at(begin + 1);
+  uint4 raw_next = rs.load(item_next, 0);
   for (int idx = begin; idx <= end && ok; ++idx) {
-    int item = -1;
-    if (idx < end) {
-      item = p.worklist[idx];
-      if (item < 0 || item >= p.n_items) {
-        if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
-        continue;
-      }
+    const int item = item_next;
+    const uint4 raw0 = raw_next;
+    item_next = item_after;
+    item_after = item_at(idx + 2);
+    if (idx < end && (item < 0 || item >= p.n_items)) {
+      if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+      raw_next = rs.load(item_next, 0);
+      continue;
     }
     int n = 0, diag = 0, limit = 0;
-    const uint8_t* row = nullptr;
+    uint32_t bits0 = 0;
     long long kv_row0 = 0;
     if (item >= 0) {
       const int qb = item % p.nQ;
-      const long long bh = item / p.nQ;
-      kv_row0 = bh * p.S;
-      row = p.mask + (long long)item * p.nK;
-      limit = p.causal ? min(p.nK, qb + 1) : p.nK;
-      for (int c0 = 0; c0 < limit; c0 += 128) {
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int col = c0 + 32 * uu + lane;
-          const bool dense = col < limit && row[col] != 0;
-          n += __popc(__ballot_sync(0xffffffffu, dense));
-        }
-      }
-      diag = p.causal && row[qb] != 0;
+      kv_row0 = (long long)(item / p.nQ) * p.S;
+      limit = rs.limit(item);
+      bits0 = rs.bits(raw0, 0, limit);
+      n = __reduce_add_sync(kAll, __popc(bits0));
+      for (int c0 = 512; c0 < limit; c0 += 512)
+        n += __reduce_add_sync(kAll, __popc(rs.bits(rs.load(item, c0), c0, limit)));
+      diag = p.causal && p.mask[(long long)item * p.nK + qb] != 0;
     }
     // publish the item
     const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
@@ -211,9 +274,10 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
         mbar_arrive(smem_u32(&c->item_full[slot]));
       }
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    ok = __shfl_sync(kAll, ok, 0);
     ++item_cnt;
     if (!ok || item < 0) break;
+    raw_next = rs.load(item_next, 0);
     if (n == 0) continue;
     if (lane == 0) {
       const uint32_t qs = q_cnt % C::kQBufs, qu = q_cnt / C::kQBufs;
@@ -228,32 +292,32 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
       }
       ++q_cnt;
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    ok = __shfl_sync(kAll, ok, 0);
     if (!ok) break;
+    // dense K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
     int prev = -1;
-    for (int c0 = 0; c0 < limit && ok; c0 += 128) {
-      unsigned bits[4];
-#pragma unroll
-      for (int uu = 0; uu < 4; ++uu) {
-        const int col = c0 + 32 * uu + lane;
-        bits[uu] = __ballot_sync(0xffffffffu, col < limit && row[col] != 0);
-      }
+    for (int c0 = 0; c0 < limit && ok; c0 += 512) {
+      const uint32_t b = c0 == 0 ? bits0 : rs.bits(rs.load(item, c0), c0, limit);
+      c->scan_bits[lane] = (uint16_t)b;
+      __syncwarp();
       if (lane == 0) {
-        for (int uu = 0; uu < 4 && ok; ++uu) {
-          unsigned b = bits[uu];
-          while (b && ok) {
-            const int col = c0 + 32 * uu + (__ffs(b) - 1);
-            b &= b - 1;
+        const uint32_t* words = reinterpret_cast<const uint32_t*>(c->scan_bits);
+        for (int w = 0; w < 16 && ok; ++w) {
+          uint32_t wb = words[w];  // columns c0 + 32 w + [0, 32)
+          while (wb && ok) {
+            const int col = c0 + 32 * w + (__ffs(wb) - 1);
+            wb &= wb - 1;
             ok = issue_tile(tk, (int)(kv_row0 + (long long)col * BLOCK));
             if (ok && prev >= 0) ok = issue_tile(tv, (int)(kv_row0 + (long long)prev * BLOCK));
             prev = col;
           }
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = __shfl_sync(kAll, ok, 0);
+      __syncwarp();
     }
     if (lane == 0 && ok) ok = issue_tile(tv, (int)(kv_row0 + (long long)prev * BLOCK));
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    ok = __shfl_sync(kAll, ok, 0);
   }
   // teardown: let every copy this CTA started land before shared memory goes away
   if (lane == 0) {
@@ -397,9 +461,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     if (n == 0) {
       if (row_ok) {
         if (partial) {
-          float4* o = reinterpret_cast<float4*>(p.o_part + grow * D + half * DW);
-#pragma unroll
-          for (int i = 0; i < DW / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          // (m, l) = (-inf, 0) marks the partial empty; its O rows are never read
           if (half == 0) { p.m_part[grow] = -INFINITY; p.l_part[grow] = 0.f; }
         } else {
           uint4* o = reinterpret_cast<uint4*>(p.out + grow * D + half * DW);

@@ -21,6 +21,7 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kChunk = 8;  // shards whose loads are in flight together
 
 __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
     const float* __restrict__ o_parts, const float* __restrict__ m_parts,
@@ -42,15 +43,35 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
     if (mstar > -INFINITY) {
-      // pass 2: weighted sums
-      for (int k = 0; k < n_shards; ++k) {
-        const float mk = __ldg(m_parts + (long long)k * rows + row);
-        const float lk = __ldg(l_parts + (long long)k * rows + row);
-        if (!(lk > 0.f && mk > -INFINITY)) continue;
-        const float wk = expf(mk - mstar);
-        const float4 o = __ldcs(reinterpret_cast<const float4*>(o_parts + ((long long)k * rows + row) * d) + c4);
-        l += wk * lk;
-        acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
+      // pass 2, kChunk shards at a time: the weights first, then the chunk's
+      // partial loads as independent predicated streams (no load waits on
+      // another), then the weighted sums.
+      for (int k0 = 0; k0 < n_shards; k0 += kChunk) {
+        float w[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          const int k = k0 + j;
+          w[j] = 0.f;
+          if (k < n_shards) {
+            const float mk = __ldg(m_parts + (long long)k * rows + row);
+            const float lk = __ldg(l_parts + (long long)k * rows + row);
+            if (lk > 0.f && mk > -INFINITY) {
+              w[j] = expf(mk - mstar);
+              l += w[j] * lk;
+            }
+          }
+        }
+        float4 o[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (w[j] > 0.f)
+            o[j] = __ldcs(reinterpret_cast<const float4*>(o_parts + ((long long)(k0 + j) * rows + row) * d) + c4);
+        }
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          acc.x += w[j] * o[j].x; acc.y += w[j] * o[j].y; acc.z += w[j] * o[j].z; acc.w += w[j] * o[j].w;
+        }
       }
       const float inv = 1.f / l;
       acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;

@@ -81,16 +81,6 @@ __device__ void block_exclusive_scan(int* a, int n, int* warp_sums) {
   __syncthreads();
 }
 
-// Number of keys < v in the ascending range a[lo, hi).
-__device__ __forceinline__ int count_below(const long long* a, int lo, int hi, long long v) {
-  int l = lo, h = hi;
-  while (l < h) {
-    const int mid = (l + h) >> 1;
-    if (a[mid] < v) l = mid + 1; else h = mid;
-  }
-  return l - lo;
-}
-
 template <int KMAX>
 __device__ __forceinline__ long long lane_minimum(const long long (&key)[KMAX]) {
   long long m = key[0];

@@ -155,7 +155,8 @@ def test_partial_mode(built_library, cuda_device, block, d, causal):
     o_ref, m_ref, l_ref = A.attention_partials(to64(q), to64(k), to64(v), mask_np, block, causal)
     m_g, l_g, o_g = to64(m_part), to64(l_part), to64(o_part)
     empty = ~np.isfinite(m_ref)
-    assert (m_g[empty] == -np.inf).all() and (l_g[empty] == 0).all() and (o_g[empty] == 0).all()
+    # o_part rows of empty partials are documented as unwritten: only (m, l) mark them
+    assert (m_g[empty] == -np.inf).all() and (l_g[empty] == 0).all()
     live = ~empty
     assert np.abs(m_g[live] - m_ref[live]).max() <= 1e-3
     assert (np.abs(l_g[live] / l_ref[live] - 1) <= 1e-2).all()
