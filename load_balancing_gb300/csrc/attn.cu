@@ -7,31 +7,33 @@
 // partial (O, m, l) of one KV shard. Causal (6D attention notes §2.3): blocks
 // above the diagonal are skipped and the diagonal block is masked per element.
 //
-// Design (one persistent CTA per worker, 10 warps):
-//   warp 0      producer: reads the item's mask row 16 bytes per lane (the next
-//               item's first 512 columns are fetched while the current item's tiles
-//               are issued), publishes the item (id, dense count) and issues TMA
-//               loads of the Q tile (two Q buffers, so the next item's Q lands during
-//               the current item) and of ONLY the dense K/V tiles into a ring of
-//               shared-memory stages, in the order the MMA warp consumes them:
-//               K0, K1, V0, K2, V1, ...
-//   warp 1      TMEM owner (512 columns: S0 | S1 | O | P); lane 0 issues
-//               tcgen05.mma: S = Q K^T (both operands in shared memory) into one of
-//               two TMEM S buffers, and O += P V with P read from TMEM and V from
-//               shared memory (MN-major), each batch committed to an mbarrier.
-//   warps 2..9  softmax, two warpgroups: thread = query row (TMEM lane); warps 2..5
-//               own the left half of the S columns and of the O columns, warps 6..9
-//               the right halves. tcgen05.ld of the half row, diagonal masking, the
-//               half-row maxima are exchanged through shared memory so both halves
-//               share one running maximum (base-2 units); P = exp2(S*scale*log2e - m)
-//               rounded to bf16 pairs and stored into the TMEM P columns with
-//               tcgen05.st; the O accumulator is rescaled in TMEM only when a row's
-//               maximum grows by more than 2^8 (the result is exact either way: O and
-//               l always share one reference maximum). Then the epilogue (O / l, LSE,
-//               or the partial triple with the true row maximum; an empty partial
-//               writes only m = -inf, l = 0).
-// Pipelining: S(j+1) is computed while the softmax of block j runs; PV(j) runs
-// while the softmax of block j+1 runs.
+// Design: one persistent CTA per worker walking its worklist; dense blocks are
+// numbered G = 0, 1, ... across the worker's items. TMEM holds the O accumulator and
+// THREE S buffers (O | S0 | S1 | S2), and P(G) is written over the first block/2
+// columns of its own S buffer, so S(G+1) and S(G+2) run on the tensor core while
+// the softmax of block G works, and the next P never waits for the previous PV.
+// 12 warps:
+//   warp 0      producer of Q and K: reads each item's mask row 16 bytes per lane,
+//               publishes (id, dense count), TMA-loads the Q tile (two buffers) and
+//               the dense K tiles into a ring;
+//   warp 1      producer of V: walks the same items and loads the dense V tiles into
+//               a second ring (S runs ahead of PV, so K and V are consumed at
+//               different times);
+//   warp 2      TMEM owner; lane 0 issues S(G) = Q K_G^T (tcgen05.mma M=128
+//               N=block K=d, both operands in shared memory) into buffer G mod 3,
+//               once PV(G-3) has completed;
+//   warp 3      lane 0 issues O += P(G) V_G (M=128 N=d K=block, P from TMEM, V from
+//               shared memory, MN-major) once the softmax has stored P(G);
+//   warps 4..7  softmax of S columns [0, block/2) and O columns [0, d/2); warps 8..11
+//               of the other halves. Thread = query row = TMEM lane. tcgen05.ld of
+//               the half row, diagonal masking, the half-row maxima are exchanged
+//               through shared memory (bounded mbarrier) so both halves share one
+//               running maximum (base-2 units); P = exp2(S*scale*log2e - m) rounded
+//               to bf16 pairs and stored into TMEM with tcgen05.st. O is rescaled in
+//               TMEM only when a row's maximum grows by more than 2^8 (exact either
+//               way: O and l always share one reference maximum), after waiting for
+//               the previous PV. Epilogue: O / l and LSE, or the partial triple with
+//               the true row maximum; an empty partial writes only m = -inf, l = 0.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer). On expiry the CTA sets the
 // device error word to DBSP_ERR_TIMEOUT, every role leaves its loop, in-flight
@@ -51,10 +53,22 @@ namespace {
 
 using namespace dbsp::ptx;
 
-constexpr int kThreads = 320;  // producer, MMA, 2 x 4 softmax warps
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;    // warpgroup 0: 2 producers, 2 MMA issuers; 2 softmax warpgroups
+constexpr int kMmaWarp = 2;
+constexpr int kSoftmaxWarp0 = 4;
+// Register split per SM sub-partition (one warp of each warpgroup): the launch gives
+// every warp 168 registers (65536 / 384, rounded down to 8); warpgroup 0 gives back
+// down to 104 and each softmax warpgroup grows to 200 (104 + 200 + 200 = 3 x 168).
+constexpr uint32_t kRegsControl = 104;
+constexpr uint32_t kRegsSoftmax = 200;
+static_assert(kRegsControl + 2 * kRegsSoftmax <= 3 * 168, "register split exceeds the launch budget");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;
-constexpr uint32_t kPCol = 384;  // P (bf16 pairs): the A operand of O += P V
+constexpr int kSBufs = 3;                // S buffers at TMEM columns 128, 256, 384
+constexpr uint32_t kSCol = 128;
+constexpr int kQBufs = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;    // 100 ms per teardown wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: P <= 256 between rescales
@@ -77,43 +91,39 @@ struct AttnParams {
 
 template <int BLOCK, int D>
 struct Cfg {
-  static constexpr int kM = 128;                          // MMA rows (query tile)
-  static constexpr int kChunk128 = 128 * 128;             // 128 rows x 128 B
+  static constexpr int kChunk128 = 128 * 128;             // 128 rows x 128 B (one 64-column chunk)
   static constexpr int kQBytes = (D / 64) * kChunk128;
   static constexpr int kTileChunk = BLOCK * 128;          // BLOCK rows x 128 B
   static constexpr int kTileBytes = (D / 64) * kTileChunk;
-  static constexpr int kTx = BLOCK * D * 2;               // bytes per Q / K / V tile load
-  static constexpr int kBudget = 200 * 1024;
-  static constexpr int kQBufs = 2;                        // the next item's Q lands during this one
-  static constexpr int kStagesFit = (kBudget - kQBufs * kQBytes) / kTileBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kDataBytes = kQBufs * kQBytes + kStages * kTileBytes;
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(kM, BLOCK, 0, 0);
-  static constexpr uint32_t kIdescPV = idesc_bf16_f32(kM, D, 0, 1);
-  static_assert(kStages >= 2, "ring too small");
+  static constexpr int kTx = BLOCK * D * 2;               // bytes of one Q / K / V tile load
+  static constexpr int kKOff = kQBufs * kQBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kDataBytes = kVOff + kVStages * kTileBytes;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, BLOCK, 0, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+  static_assert(D <= 128 && BLOCK <= 128, "shape");
 };
 
 struct alignas(8) Ctrl {
-  uint64_t q_full[2], q_empty[2];
-  uint64_t ring_full[8], ring_empty[8];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done;
+  uint64_t q_full[kQBufs], q_empty[kQBufs];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t item_full[2], item_empty[2];
-  uint64_t drain;
   uint64_t xbar[2], lbar[2];      // row-max (per block) and row-sum (per item) exchange
-  float xmax[2][2][128];          // [block parity][column half][row]
-  float xsum[2][2][128];          // [item parity][column half][row]
+  uint64_t drain;
   int item_id[2], item_n[2], item_diag[2];
-  alignas(4) uint16_t scan_bits[32];  // producer: dense bits of one 512-column mask chunk
+  alignas(4) uint16_t scan_bits[2][32];  // producers: dense bits of one 512-column mask chunk
   uint32_t tmem_base;
   volatile int abort_flag;
   long long blocks_done;
+  float xmax[2][2][128];          // [block parity][column half][row]
+  float xsum[2][2][128];          // [item parity][column half][row]
 };
 
 template <int BLOCK, int D>
 constexpr size_t smem_bytes() {
-  size_t s = 1024 + Cfg<BLOCK, D>::kDataBytes + sizeof(Ctrl) + 64;
-  return s < 136 * 1024 ? 136 * 1024 : s;  // one CTA (one TMEM owner) per SM; slack after the ring
+  return 1024 + Cfg<BLOCK, D>::kDataBytes + sizeof(Ctrl);
 }
 
 // Bounded wait. Returns false on timeout or when another role has aborted.
@@ -152,7 +162,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ producers
 // 4-bit mask of the non-zero bytes of x (bit i <-> byte i).
 __device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
   const uint32_t t = __vcmpne4(x, 0u) & 0x01010101u;
@@ -171,230 +181,229 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* ptr) {
 // lane when every row starts on a 16-byte boundary, else byte by byte.
 struct RowScan {
   const uint8_t* mask;
-  int nK, nQ, causal, n_items;
+  int nK, nQ, causal;
   bool vec;
   int lane;
 
   __device__ int limit(int item) const {
     return causal ? min(nK, item % nQ + 1) : nK;
   }
-  // raw bytes of the lane's 16 columns of chunk c0 (zero where col >= limit)
-  __device__ uint4 load(int item, int c0) const {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (item < 0 || item >= n_items) return v;
-    const int lim = limit(item), col = c0 + 16 * lane;
-    if (col >= lim) return v;
-    const uint8_t* row = mask + (long long)item * nK;
-    if (vec) return ld_nc_v4(row + col);  // col + 16 <= nK: nK is a multiple of 16
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    for (int t = 0; t < 16 && col + t < lim; ++t) w[t >> 2] |= (uint32_t)row[col + t] << (8 * (t & 3));
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  // dense-block bits of those columns, limited to col < lim
-  __device__ uint32_t bits(uint4 v, int c0, int lim) const {
-    const int rem = lim - (c0 + 16 * lane);
+  // dense-block bits of the lane's 16 columns of chunk c0, limited to col < lim
+  __device__ uint32_t bits(int item, int c0, int lim) const {
+    const int col = c0 + 16 * lane;
+    const int rem = lim - col;
     if (rem <= 0) return 0u;
-    uint32_t b = nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4) | (nonzero_bytes(v.z) << 8) |
-                 (nonzero_bytes(v.w) << 12);
+    const uint8_t* row = mask + (long long)item * nK;
+    uint32_t b = 0;
+    if (vec) {  // col + 16 <= nK: nK is a multiple of 16
+      const uint4 v = ld_nc_v4(row + col);
+      b = nonzero_bytes(v.x) | (nonzero_bytes(v.y) << 4) | (nonzero_bytes(v.z) << 8) |
+          (nonzero_bytes(v.w) << 12);
+    } else {
+      for (int t = 0; t < 16 && t < rem; ++t) b |= (row[col + t] != 0 ? 1u : 0u) << t;
+    }
     return rem < 16 ? b & ((1u << rem) - 1u) : b;
   }
 };
 
+// Producer warp `which` (0: Q and K, 1: V). Both walk the worker's items in list
+// order; producer 0 also publishes every item to the MMA issuer and the softmax
+// warps. `each(col)` is called by lane 0 for the dense blocks of the row, in order.
 template <int BLOCK, int D>
-__device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                             const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sRing, int worker) {
+__device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                             const AttnParams& p, Ctrl* c, uint8_t* data) {
   using C = Cfg<BLOCK, D>;
   constexpr unsigned kAll = 0xffffffffu;
   const int lane = threadIdx.x & 31;
-  int begin = p.offsets[worker], end = p.offsets[worker + 1];
-  if (begin < 0 || end < begin) {
-    if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
-    begin = end = 0;
-  }
   RowScan rs;
   rs.mask = p.mask;
   rs.nK = p.nK;
   rs.nQ = p.nQ;
   rs.causal = p.causal;
-  rs.n_items = p.n_items;
   rs.vec = ((reinterpret_cast<uintptr_t>(p.mask) | (uintptr_t)p.nK) & 15u) == 0;
   rs.lane = lane;
-  uint32_t item_cnt = 0, q_cnt = 0, ring_cnt = 0;
+  int begin = p.offsets[blockIdx.x], end = p.offsets[blockIdx.x + 1];
+  if (begin < 0 || end < begin) {
+    if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+    begin = end = 0;
+  }
+  uint32_t item_cnt = 0, q_cnt = 0, t_cnt = 0;  // items published, Q tiles, K or V tiles issued
+  const int kstages = which == 0 ? kKStages : kVStages;
+  uint64_t* full = which == 0 ? c->k_full : c->v_full;
+  uint64_t* empty = which == 0 ? c->k_empty : c->v_empty;
+  const uint32_t ring = smem_u32(data + (which == 0 ? C::kKOff : C::kVOff));
+  const CUtensorMap* map = which == 0 ? tk : tv;
   bool ok = true;
-  // q/k/v tile issue (lane 0 only)
-  auto issue_tile = [&](const CUtensorMap* map, int row) -> bool {
-    const uint32_t s = ring_cnt % C::kStages, u = ring_cnt / C::kStages;
-    const uint32_t full = smem_u32(&c->ring_full[s]);
-    if (!wait_bar(c, smem_u32(&c->ring_empty[s]), (u & 1) ^ 1, p.err)) return false;
-    mbar_arrive_expect_tx(full, C::kTx);
-    const uint32_t dst = smem_u32(sRing + s * C::kTileBytes);
-#pragma unroll
-    for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kTileChunk, map, ch * 64, row, full);
-    ++ring_cnt;
-    return true;
-  };
-  auto item_at = [&](int idx) -> int { return idx < end ? __ldg(p.worklist + idx) : -1; };
-
-  // Item ids run two entries ahead and the first mask chunk one item ahead, so their
-  // load latency hides under the previous item's tile issue.
-  int item_next = item_at(begin);
-  int item_after = item_at(begin + 1);
-  uint4 raw_next = rs.load(item_next, 0);
   for (int idx = begin; idx <= end && ok; ++idx) {
-    const int item = item_next;
-    const uint4 raw0 = raw_next;
-    item_next = item_after;
-    item_after = item_at(idx + 2);
-    if (idx < end && (item < 0 || item >= p.n_items)) {
-      if (lane == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
-      raw_next = rs.load(item_next, 0);
-      continue;
+    int item = -1;
+    if (idx < end) {
+      item = __ldg(p.worklist + idx);
+      if (item < 0 || item >= p.n_items) {
+        if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+        continue;
+      }
     }
-    int n = 0, diag = 0, limit = 0;
-    uint32_t bits0 = 0;
+    int n = 0, limit = 0;
     long long kv_row0 = 0;
     if (item >= 0) {
-      const int qb = item % p.nQ;
       kv_row0 = (long long)(item / p.nQ) * p.S;
       limit = rs.limit(item);
-      bits0 = rs.bits(raw0, 0, limit);
-      n = __reduce_add_sync(kAll, __popc(bits0));
-      for (int c0 = 512; c0 < limit; c0 += 512)
-        n += __reduce_add_sync(kAll, __popc(rs.bits(rs.load(item, c0), c0, limit)));
-      diag = p.causal && p.mask[(long long)item * p.nK + qb] != 0;
+      if (which == 0)
+        for (int c0 = 0; c0 < limit; c0 += 512) n += __reduce_add_sync(kAll, __popc(rs.bits(item, c0, limit)));
     }
-    // publish the item
-    const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
-    if (lane == 0) {
-      ok = wait_bar(c, smem_u32(&c->item_empty[slot]), (su & 1) ^ 1, p.err);
-      if (ok) {
-        c->item_id[slot] = item;
-        c->item_n[slot] = n;
-        c->item_diag[slot] = diag;
-        mbar_arrive(smem_u32(&c->item_full[slot]));
+    if (which == 0) {  // publish the item
+      const int diag = item >= 0 && p.causal && p.mask[(long long)item * p.nK + item % p.nQ] != 0;
+      const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
+      if (lane == 0) {
+        ok = wait_bar(c, smem_u32(&c->item_empty[slot]), (su & 1) ^ 1, p.err);
+        if (ok) {
+          c->item_id[slot] = item;
+          c->item_n[slot] = n;
+          c->item_diag[slot] = diag;
+          mbar_arrive(smem_u32(&c->item_full[slot]));
+        }
       }
-    }
-    ok = __shfl_sync(kAll, ok, 0);
-    ++item_cnt;
-    if (!ok || item < 0) break;
-    raw_next = rs.load(item_next, 0);
-    if (n == 0) continue;
-    if (lane == 0) {
-      const uint32_t qs = q_cnt % C::kQBufs, qu = q_cnt / C::kQBufs;
-      ok = wait_bar(c, smem_u32(&c->q_empty[qs]), (qu & 1) ^ 1, p.err);
-      if (ok) {
-        const uint32_t full = smem_u32(&c->q_full[qs]);
-        mbar_arrive_expect_tx(full, C::kTx);
-        const int qrow = (int)(kv_row0 + (long long)(item % p.nQ) * BLOCK);
-        const uint32_t dst = smem_u32(sQ + qs * C::kQBytes);
+      ok = __shfl_sync(kAll, ok, 0);
+      ++item_cnt;
+      if (!ok || item < 0) break;
+      if (n == 0) continue;
+      if (lane == 0) {  // the Q tile of this item
+        const uint32_t qs = q_cnt % kQBufs, qu = q_cnt / kQBufs;
+        ok = wait_bar(c, smem_u32(&c->q_empty[qs]), (qu & 1) ^ 1, p.err);
+        if (ok) {
+          const uint32_t qf = smem_u32(&c->q_full[qs]);
+          mbar_arrive_expect_tx(qf, C::kTx);
+          const int qrow = (int)(kv_row0 + (long long)(item % p.nQ) * BLOCK);
+          const uint32_t dst = smem_u32(data) + qs * C::kQBytes;
 #pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kChunk128, tq, ch * 64, qrow, full);
+          for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kChunk128, tq, ch * 64, qrow, qf);
+        }
+        ++q_cnt;
       }
-      ++q_cnt;
+      ok = __shfl_sync(kAll, ok, 0);
+      if (!ok) break;
+    } else if (item < 0) {
+      break;
     }
-    ok = __shfl_sync(kAll, ok, 0);
-    if (!ok) break;
-    // dense K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
-    int prev = -1;
+    // the dense K (or V) tiles of the row, in block order
     for (int c0 = 0; c0 < limit && ok; c0 += 512) {
-      const uint32_t b = c0 == 0 ? bits0 : rs.bits(rs.load(item, c0), c0, limit);
-      c->scan_bits[lane] = (uint16_t)b;
+      c->scan_bits[which][lane] = (uint16_t)rs.bits(item, c0, limit);
       __syncwarp();
       if (lane == 0) {
-        const uint32_t* words = reinterpret_cast<const uint32_t*>(c->scan_bits);
+        const uint32_t* words = reinterpret_cast<const uint32_t*>(c->scan_bits[which]);
         for (int w = 0; w < 16 && ok; ++w) {
           uint32_t wb = words[w];  // columns c0 + 32 w + [0, 32)
           while (wb && ok) {
             const int col = c0 + 32 * w + (__ffs(wb) - 1);
             wb &= wb - 1;
-            ok = issue_tile(tk, (int)(kv_row0 + (long long)col * BLOCK));
-            if (ok && prev >= 0) ok = issue_tile(tv, (int)(kv_row0 + (long long)prev * BLOCK));
-            prev = col;
+            const uint32_t s = t_cnt % kstages, u = t_cnt / kstages;
+            ok = wait_bar(c, smem_u32(&empty[s]), (u & 1) ^ 1, p.err);
+            if (ok) {
+              const uint32_t f = smem_u32(&full[s]);
+              mbar_arrive_expect_tx(f, C::kTx);
+              const uint32_t dst = ring + s * C::kTileBytes;
+              const int row = (int)(kv_row0 + (long long)col * BLOCK);
+#pragma unroll
+              for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kTileChunk, map, ch * 64, row, f);
+              ++t_cnt;
+            }
           }
         }
       }
       ok = __shfl_sync(kAll, ok, 0);
       __syncwarp();
     }
-    if (lane == 0 && ok) ok = issue_tile(tv, (int)(kv_row0 + (long long)prev * BLOCK));
-    ok = __shfl_sync(kAll, ok, 0);
   }
-  // teardown: let every copy this CTA started land before shared memory goes away
+  // teardown: let every copy this warp started land before shared memory goes away
   if (lane == 0) {
-    const uint32_t issued = ring_cnt;
-    for (uint32_t k = issued > (uint32_t)C::kStages ? issued - C::kStages : 0; k < issued; ++k)
-      drain_bar(smem_u32(&c->ring_full[k % C::kStages]), (k / C::kStages) & 1);
-    for (uint32_t k = q_cnt > (uint32_t)C::kQBufs ? q_cnt - C::kQBufs : 0; k < q_cnt; ++k)
-      drain_bar(smem_u32(&c->q_full[k % C::kQBufs]), (k / C::kQBufs) & 1);
+    for (uint32_t k = t_cnt > (uint32_t)kstages ? t_cnt - kstages : 0; k < t_cnt; ++k)
+      drain_bar(smem_u32(&full[k % kstages]), (k / kstages) & 1);
+    for (uint32_t k = q_cnt > (uint32_t)kQBufs ? q_cnt - kQBufs : 0; k < q_cnt; ++k)
+      drain_bar(smem_u32(&c->q_full[k % kQBufs]), (k / kQBufs) & 1);
   }
   __syncwarp();
 }
 
-// ------------------------------------------------------------------ MMA issuer
+// ------------------------------------------------------------------ MMA issuers
+// Two threads issue tcgen05.mma: one the S products, one the PV products. An MMA
+// issue holds its thread for about the MMA's duration, so every mbarrier test or
+// commit of a single issuer would leave the tensor core idle; with two issuers one
+// thread's synchronisation overlaps the other's MMAs. tcgen05.commit tracks the MMAs
+// of the committing thread, which is all each barrier below needs.
+
+// S(G) = Q K_G^T into S buffer G mod 3, once PV(G-3) has released that buffer.
 template <int BLOCK, int D>
-__device__ void run_mma(const AttnParams& p, Ctrl* c, uint8_t* sQ, uint8_t* sRing,
-                        uint32_t tmem) {
+__device__ void run_mma_s(const AttnParams& p, Ctrl* c, uint32_t data, uint32_t tmem) {
   using C = Cfg<BLOCK, D>;
-  uint32_t item_cnt = 0, q_cnt = 0, ring_cnt = 0, g = 0;
-  long long blocks = 0;
+  uint32_t items = 0, G = 0, ks = 0, qc = 0;
   bool ok = true;
-  const uint32_t q_base = smem_u32(sQ), ring_addr = smem_u32(sRing);
   while (ok) {
-    const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
-    if (!wait_bar(c, smem_u32(&c->item_full[slot]), su & 1, p.err)) break;
+    const uint32_t slot = items & 1;
+    if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
     const int item = c->item_id[slot], n = c->item_n[slot];
-    mbar_arrive(smem_u32(&c->item_empty[slot]));
-    ++item_cnt;
+    ++items;  // the PV issuer, which is behind, releases the slot
     if (item < 0) break;
     if (n == 0) continue;
-    const uint32_t qs = q_cnt % C::kQBufs;
-    if (!wait_bar(c, smem_u32(&c->q_full[qs]), (q_cnt / C::kQBufs) & 1, p.err)) break;
-    ++q_cnt;
-    const uint32_t q_addr = q_base + qs * C::kQBytes;
-    for (int jj = 0; jj <= n && ok; ++jj) {
-      if (jj < n) {  // S(g + jj) = Q K^T
-        const uint32_t gg = g + jj, sb = gg & 1;
-        const uint32_t s = ring_cnt % C::kStages, u = ring_cnt / C::kStages;
-        ok = wait_bar(c, smem_u32(&c->s_free[sb]), ((gg >> 1) & 1) ^ 1, p.err) &&
-             wait_bar(c, smem_u32(&c->ring_full[s]), u & 1, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kt = ring_addr + s * C::kTileBytes;
+    const uint32_t qs = qc % kQBufs;
+    if (!wait_bar(c, smem_u32(&c->q_full[qs]), (qc / kQBufs) & 1, p.err)) break;
+    const uint32_t qa = data + qs * C::kQBytes;
+    for (int j = 0; j < n && ok; ++j, ++G, ++ks) {
+      const uint32_t b = G % kSBufs, kst = ks % kKStages;
+      ok = (G < (uint32_t)kSBufs || wait_bar(c, smem_u32(&c->pv_done[b]), ((G / kSBufs) - 1) & 1, p.err)) &&
+           wait_bar(c, smem_u32(&c->k_full[kst]), (ks / kKStages) & 1, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t kb = data + C::kKOff + kst * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(q_addr + (kk >> 2) * C::kChunk128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(kt + (kk >> 2) * C::kTileChunk + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + sb * 128, a, b, C::kIdescS, kk > 0);
-        }
-        mma_commit(smem_u32(&c->ring_empty[s]));
-        mma_commit(smem_u32(&c->s_full[sb]));
-        if (jj == n - 1) mma_commit(smem_u32(&c->q_empty[qs]));
-        ++ring_cnt;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t a = smem_desc_sw128(qa + (kk >> 2) * C::kChunk128 + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kTileChunk + (kk & 3) * 32, 16, 1024);
+        mma_bf16_ss(tmem + kSCol + b * 128, a, bd, C::kIdescS, kk > 0);
       }
-      if (jj > 0) {  // O (+)= P V for block g + jj - 1
-        const uint32_t gp = g + jj - 1;
-        const uint32_t s = ring_cnt % C::kStages, u = ring_cnt / C::kStages;
-        ok = wait_bar(c, smem_u32(&c->p_full), gp & 1, p.err) &&
-             wait_bar(c, smem_u32(&c->ring_full[s]), u & 1, p.err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vt = ring_addr + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < BLOCK / 16; ++kk) {
-          const uint64_t b = smem_desc_sw128(vt + kk * 16 * 128, C::kTileChunk, 1024);
-          mma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, b, C::kIdescPV, (jj > 1 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&c->ring_empty[s]));
-        mma_commit(smem_u32(&c->pv_done));
-        ++ring_cnt;
-      }
+      mma_commit(smem_u32(&c->k_empty[kst]));
+      mma_commit(smem_u32(&c->s_full[b]));
     }
-    g += n;
-    blocks += n;
+    if (!ok) break;
+    mma_commit(smem_u32(&c->q_empty[qs]));
+    ++qc;
   }
   // teardown: every MMA issued by this thread must finish before TMEM is freed
   mma_commit(smem_u32(&c->drain));
-  drain_bar(smem_u32(&c->drain), 0);
+}
+
+// O (+)= P(G) V_G once the softmax has stored P(G); releases the item slots.
+template <int BLOCK, int D>
+__device__ void run_mma_pv(const AttnParams& p, Ctrl* c, uint32_t data, uint32_t tmem) {
+  using C = Cfg<BLOCK, D>;
+  uint32_t items = 0, G = 0, vs = 0;
+  long long blocks = 0;
+  bool ok = true;
+  while (ok) {
+    const uint32_t slot = items & 1;
+    if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
+    const int item = c->item_id[slot], n = c->item_n[slot];
+    mbar_arrive(smem_u32(&c->item_empty[slot]));
+    ++items;
+    if (item < 0) break;
+    for (int j = 0; j < n && ok; ++j, ++G, ++vs) {
+      const uint32_t b = G % kSBufs, vst = vs % kVStages;
+      ok = wait_bar(c, smem_u32(&c->p_full[b]), (G / kSBufs) & 1, p.err) &&
+           wait_bar(c, smem_u32(&c->v_full[vst]), (vs / kVStages) & 1, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t vb = data + C::kVOff + vst * C::kTileBytes;
+      const uint32_t pcol = tmem + kSCol + b * 128;
+#pragma unroll
+      for (int kk = 0; kk < BLOCK / 16; ++kk) {
+        const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, C::kTileChunk, 1024);
+        mma_bf16_ts(tmem, pcol + kk * 8, bd, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&c->v_empty[vst]));
+      mma_commit(smem_u32(&c->pv_done[b]));
+      ++blocks;
+    }
+  }
+  mma_commit(smem_u32(&c->drain));
   c->blocks_done = blocks;
 }
 
@@ -428,8 +437,8 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Softmax warpgroups: warps 2..5 own columns [0, BLOCK/2) of every S row and columns
-// [0, D/2) of O; warps 6..9 own the other halves. Both halves of a row see the
+// Softmax warpgroups: warps 4..7 own columns [0, BLOCK/2) of every S row and columns
+// [0, D/2) of O; warps 8..11 own the other halves. Both halves of a row see the
 // same row maximum through a shared-memory exchange behind a bounded mbarrier, so
 // their rescale decisions agree; the row sum is combined once per item.
 template <int BLOCK, int D>
@@ -438,22 +447,22 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
   constexpr int DW = D / 2;      // O columns per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int half = (warp - 2) >> 2;
+  const int half = (warp - kSoftmaxWarp0) >> 2;
   const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
   const bool row_ok = r < BLOCK;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-  const uint32_t s_off = half * CW, o_off = kOCol + half * DW, p_off = kPCol + half * (CW / 2);
+  const uint32_t o_off = half * DW;
   const bool partial = p.o_part != nullptr;
   const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
-  uint32_t item_cnt = 0, g = 0, items_done = 0;
+  uint32_t items = 0, G = 0, items_done = 0;
   bool ok = true;
   while (ok) {
-    const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
-    if (!wait_bar(c, smem_u32(&c->item_full[slot]), su & 1, p.err)) break;
+    const uint32_t slot = items & 1;
+    if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
     const int item = c->item_id[slot], n = c->item_n[slot], diag = c->item_diag[slot];
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&c->item_empty[slot]));
-    ++item_cnt;
+    ++items;
     if (item < 0) break;
     const long long bh = item / p.nQ;
     const int qb = item % p.nQ;
@@ -473,44 +482,43 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
       continue;
     }
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
-    for (int jj = 0; jj < n; ++jj, ++g) {
-      const uint32_t sb = g & 1;
-      if (!wait_bar(c, smem_u32(&c->s_full[sb]), (g >> 1) & 1, p.err)) { ok = false; break; }
+    for (int j = 0; j < n; ++j, ++G) {
+      const uint32_t b = G % kSBufs, bu = G / kSBufs, xs = G & 1;
+      const uint32_t sbase = lane_base + kSCol + b * 128;
+      if (!wait_bar(c, smem_u32(&c->s_full[b]), bu & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[CW];
-      if constexpr (CW == 64) tmem_ld64_wait(lane_base + sb * 128 + s_off, sr);
-      else tmem_ld32_wait(lane_base + sb * 128 + s_off, sr);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->s_free[sb]));
-
+      if constexpr (CW == 64) tmem_ld64_wait(sbase + half * CW, sr);
+      else tmem_ld32_wait(sbase + half * CW, sr);
       float* s = reinterpret_cast<float*>(sr);
-      if (diag && jj == n - 1) {
+      if (diag && j == n - 1) {
 #pragma unroll
-        for (int k = 0; k < CW; ++k) if (s_off + k > (uint32_t)r) s[k] = -INFINITY;
+        for (int k = 0; k < CW; ++k) if (half * CW + k > r) s[k] = -INFINITY;
       }
       // half-row maximum (3-input max, 4 independent chains)
       static_assert(CW % 8 == 0, "half rows come in multiples of 8 columns");
       float mxa[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mxa[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+      for (int q = 0; q < 4; ++q) mxa[q] = fmaxf(s[2 * q], s[2 * q + 1]);
 #pragma unroll
       for (int k = 8; k < CW; k += 8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) mxa[i] = max3(mxa[i], s[k + 2 * i], s[k + 2 * i + 1]);
+        for (int q = 0; q < 4; ++q) mxa[q] = max3(mxa[q], s[k + 2 * q], s[k + 2 * q + 1]);
       }
       const float mh = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
-      c->xmax[sb][half][r] = mh;
+      c->xmax[xs][half][r] = mh;
+      tc_fence_before();  // this half's S reads precede the other half's P writes
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->xbar[sb]));
-      if (!wait_bar(c, smem_u32(&c->xbar[sb]), (g >> 1) & 1, p.err)) { ok = false; break; }
-      const float mx = fmaxf(mh, c->xmax[sb][half ^ 1][r]);
+      if (lane == 0) mbar_arrive(smem_u32(&c->xbar[xs]));
+      if (!wait_bar(c, smem_u32(&c->xbar[xs]), (G >> 1) & 1, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const float mx = fmaxf(mh, c->xmax[xs][half ^ 1][r]);
 
       float alpha = 1.f;
       bool rescale = false;
       const float mxs = mx * p.scale_log2;
       m_true = fmaxf(m_true, mxs);
-      if (jj == 0) {
+      if (j == 0) {
         m_ref = mxs;
       } else if (mxs > m_ref + kRescaleThreshold) {
         alpha = ex2(m_ref - mxs);
@@ -537,26 +545,27 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
         f2_unpack(t, t0, t1);
         l += t0 + t1;
       }
-      // P and O may be touched only once PV of the previous block is complete
-      if (!wait_bar(c, smem_u32(&c->pv_done), (g & 1) ^ 1, p.err)) { ok = false; break; }
-      tc_fence_after();
+      // P over this half's share of the first BLOCK/2 columns of the S buffer
+      if constexpr (CW == 64) tmem_st32(sbase + half * (CW / 2), pk);
+      else tmem_st16(sbase + half * (CW / 2), pk);
       if (__any_sync(0xffffffffu, rescale)) {
+        // O may be touched only once PV of the previous block is complete
+        const uint32_t gp = G - 1, pb = gp % kSBufs;
+        if (!wait_bar(c, smem_u32(&c->pv_done[pb]), (gp / kSBufs) & 1, p.err)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < DW / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32_wait(lane_base + o_off + cc * 32, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
           tmem_st32(lane_base + o_off + cc * 32, o);
         }
-        tmem_wait_st();
       }
-      if constexpr (CW == 64) tmem_st32(lane_base + p_off, pk);
-      else tmem_st16(lane_base + p_off, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[b]));
     }
     if (!ok) break;
     // row sum of both halves (once per item)
@@ -567,8 +576,10 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     if (!wait_bar(c, smem_u32(&c->lbar[lb]), (items_done >> 1) & 1, p.err)) break;
     l += c->xsum[lb][half ^ 1][r];
     ++items_done;
-    // epilogue: wait for the last PV of this item
-    if (!wait_bar(c, smem_u32(&c->pv_done), (g - 1) & 1, p.err)) break;
+    // epilogue: wait for the last PV of this item; the next item's first PV waits for
+    // these warps' P, which they store only after the reads below
+    const uint32_t gl = G - 1;
+    if (!wait_bar(c, smem_u32(&c->pv_done[gl % kSBufs]), (gl / kSBufs) & 1, p.err)) break;
     tc_fence_after();
     uint32_t o[DW];
     if constexpr (DW == 64) tmem_ld64_wait(lane_base + o_off, o);
@@ -611,33 +622,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap tv, const AttnParams p) {
   using C = Cfg<BLOCK, D>;
   extern __shared__ uint8_t smem_raw[];
+  // shared memory: Q buffers | K ring | V ring | control
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sRing = sQ + C::kQBufs * C::kQBytes;
-  Ctrl* c = reinterpret_cast<Ctrl*>(sRing + C::kStages * C::kTileBytes);
+  Ctrl* c = reinterpret_cast<Ctrl*>(base + C::kDataBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t t_start = globaltimer();
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&c->q_full[b]), 1);
-      mbar_init(smem_u32(&c->q_empty[b]), 1);
+    for (int i = 0; i < kQBufs; ++i) {
+      mbar_init(smem_u32(&c->q_full[i]), 1);
+      mbar_init(smem_u32(&c->q_empty[i]), 1);
     }
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&c->ring_full[s]), 1);
-      mbar_init(smem_u32(&c->ring_empty[s]), 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(smem_u32(&c->k_full[i]), 1);
+      mbar_init(smem_u32(&c->k_empty[i]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&c->s_full[b]), 1);
-      mbar_init(smem_u32(&c->s_free[b]), 8);
-      mbar_init(smem_u32(&c->item_full[b]), 1);
-      mbar_init(smem_u32(&c->item_empty[b]), 9);
-      mbar_init(smem_u32(&c->xbar[b]), 8);
-      mbar_init(smem_u32(&c->lbar[b]), 8);
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(smem_u32(&c->v_full[i]), 1);
+      mbar_init(smem_u32(&c->v_empty[i]), 1);
     }
-    mbar_init(smem_u32(&c->p_full), 8);
-    mbar_init(smem_u32(&c->pv_done), 1);
-    mbar_init(smem_u32(&c->drain), 1);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(smem_u32(&c->s_full[i]), 1);
+      mbar_init(smem_u32(&c->p_full[i]), 8);
+      mbar_init(smem_u32(&c->pv_done[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&c->item_full[i]), 1);
+      mbar_init(smem_u32(&c->item_empty[i]), 9);  // MMA issuer + 8 softmax warps
+      mbar_init(smem_u32(&c->xbar[i]), 8);
+      mbar_init(smem_u32(&c->lbar[i]), 8);
+    }
+    mbar_init(smem_u32(&c->drain), 2);  // one commit per MMA issuer
     c->abort_flag = 0;
     c->blocks_done = 0;
     fence_mbarrier_init();
@@ -647,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&c->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -656,19 +671,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
 
-  if (warp == 0) {
-    run_producer<BLOCK, D>(&tq, &tk, &tv, p, c, sQ, sRing, blockIdx.x);
-  } else if (warp == 1) {
-    if (lane == 0) run_mma<BLOCK, D>(p, c, sQ, sRing, tmem);
-    __syncwarp();
+  if (warp < kSoftmaxWarp0) {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp < 2) {
+      run_producer<BLOCK, D>(warp, &tq, &tk, &tv, p, c, base);
+    } else {
+      if (lane == 0) {
+        if (warp == kMmaWarp) run_mma_s<BLOCK, D>(p, c, smem_u32(base), tmem);
+        else run_mma_pv<BLOCK, D>(p, c, smem_u32(base), tmem);
+        drain_bar(smem_u32(&c->drain), 0);  // both issuers' MMAs are complete
+      }
+      __syncwarp();
+    }
   } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     run_softmax<BLOCK, D>(p, c, tmem);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && p.timing) {
     p.timing[3 * blockIdx.x + 0] = (int64_t)t_start;
     p.timing[3 * blockIdx.x + 1] = (int64_t)globaltimer();

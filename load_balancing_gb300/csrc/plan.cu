@@ -16,14 +16,14 @@
 //   phase 1  the stable order (load desc, id asc): a counting sort through a
 //            shared-memory histogram, its stable scatter done by one warp with
 //            match_any (or rank-by-comparison for n <= 16384 with large loads);
-//   phase 2  the greedy, one warp.
-//            Without a bonus it goes one RUN of equal loads w at a time, in
+//   phase 2  the greedy.
+//            Without a bonus (whole CTA) it goes one RUN of equal loads w at a time, in
 //            batches: with the workers' keys sorted ascending in A, every key
 //            below A[0] + (w << 11) is taken in order by the next items of the
 //            run -- each re-keyed worker (key + (w << 11)) is above all of
 //            them, so the one-at-a-time greedy picks exactly this sequence --
-//            then the re-keyed batch is merged back into A (binary searches).
-//            With a bonus the key of item i's home worker is lowered by the
+//            then the re-keyed batch is merged back into A (binary searches, one
+//            element per thread). With a bonus (one warp) the key of item i's home worker is lowered by the
 //            bonus for that choice only, so items go one at a time: every lane
 //            keeps the keys of workers lane, lane+32, ... in registers and the
 //            warp minimum takes two redux.sync (high word, then low word).
@@ -95,60 +95,7 @@ struct Sorted {  // the stable order, staged in shared memory or in the worklist
   __device__ __forceinline__ int operator[](int t) const { return smem ? (int)smem[t] : gmem[t]; }
 };
 
-// One merge of a batch (see greedy_batched): E = bp + tail keys are re-placed, KE per
-// lane, as straight-line code so that the KE binary searches of a lane interleave.
-template <int KE>
-__device__ __forceinline__ void merge_step(long long* A, int m, int h, int b, int bp, int E, long long step,
-                                           int iters, int h_new) {
-  const int lane = threadIdx.x & 31;
-  long long val[KE], tgt[KE];
-  int lo[KE], hi[KE];
-#pragma unroll
-  for (int t = 0; t < KE; ++t) {
-    const int k = lane + 32 * t;
-    const bool live = k < E;
-    const bool is_y = k < bp;
-    int src = is_y ? k : b + k - bp;
-    src = live ? src : 0;
-    int x = h + src;
-    x = x >= m ? x - m : x;
-    const long long a = A[x];
-    val[t] = is_y ? a + step : a;
-    tgt[t] = is_y ? val[t] : a - step;
-    lo[t] = !live ? 0 : (is_y ? b : 0);
-    hi[t] = !live ? 0 : (is_y ? m : bp);
-  }
-  for (int it = 0; it < iters; ++it) {
-#pragma unroll
-    for (int t = 0; t < KE; ++t) {
-      const int mid = (lo[t] + hi[t]) >> 1;  // lo == hi <= m still indexes the list
-      int x = h + mid;
-      x = x >= m ? x - m : x;
-      x = x >= m ? x - m : x;
-      const long long am = A[x];
-      const bool go = lo[t] < hi[t];
-      const bool less = am < tgt[t];
-      lo[t] = go && less ? mid + 1 : lo[t];
-      hi[t] = go && !less ? mid : hi[t];
-    }
-  }
-  int dst[KE];
-#pragma unroll
-  for (int t = 0; t < KE; ++t) {
-    const int k = lane + 32 * t;
-    const int pos = k < bp ? (b - bp) + k + (lo[t] - b) : (b - bp) + (k - bp) + lo[t];
-    int x = h_new + pos;
-    x = x >= m ? x - m : x;
-    dst[t] = k < E ? x : -1;
-  }
-  __syncwarp();  // all reads of the old order are done
-#pragma unroll
-  for (int t = 0; t < KE; ++t)
-    if (dst[t] >= 0) A[dst[t]] = val[t];
-  __syncwarp();
-}
-
-// Phase 2 without a bonus: batches per run of equal loads (one warp), KMAX keys per lane.
+// Phase 2 without a bonus: batches per run of equal loads, on the whole CTA.
 // The worker keys stay sorted in a circular list: logical key i is A[(h + i) mod m].
 // One batch of a run with load w (wk = w << 11), b = number of keys below
 // A[h] + wk:
@@ -159,14 +106,16 @@ __device__ __forceinline__ void merge_step(long long* A, int m, int h, int b, in
 //     for q = ceil((key1 - key0) / wk) picks, and is re-keyed once by q * wk.
 // Then the head advances past the picked keys; the keys below the threshold do not
 // move, and only the "tail" (keys at or above the threshold) is merged with the
-// re-keyed keys, each placed by a binary search in the other list.
-template <int KMAX>
-__device__ __forceinline__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbins, int max_load, int n, int m,
+// re-keyed keys: every element is placed by a binary search in the other list, KT
+// elements per thread, all searches of a batch in parallel.
+template <int KT>
+__device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbins, int max_load, int n, int m,
                                long long* A, int* counts, long long* final_load,
-                               int32_t* __restrict__ worker_of) {
-  const int lane = threadIdx.x & 31;
-  for (int j = lane; j < m; j += 32) { A[j] = j; counts[j] = 0; }
-  __syncwarp();
+                               int32_t* __restrict__ worker_of, int* red) {
+  constexpr int kW = kThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int j = tid; j < m; j += kThreads) { A[j] = j; counts[j] = 0; }
+  __syncthreads();
   int h = 0;
   auto phys = [&](int i) { const int x = h + i; return x >= m ? x - m : x; };
   int s = 0;
@@ -178,10 +127,10 @@ __device__ __forceinline__ void greedy_batched(const Sorted sorted, const int* b
     if (w == 0) {  // zero loads never change a key: they all go to the current minimum
       const int p0 = (int)(A[h] & kWorkerMask);
       const int base = counts[p0];
-      for (int j = lane; j < r; j += 32) worker_of[sorted[s + j]] = p0 + m * (base + j);
-      __syncwarp();
-      if (lane == 0) counts[p0] = base + r;
-      __syncwarp();
+      for (int j = tid; j < r; j += kThreads) worker_of[sorted[s + j]] = p0 + m * (base + j);
+      __syncthreads();
+      if (tid == 0) counts[p0] = base + r;
+      __syncthreads();
       s = e;
       continue;
     }
@@ -191,27 +140,30 @@ __device__ __forceinline__ void greedy_batched(const Sorted sorted, const int* b
       const long long thr = key0 + wk;
       int c = 0;
 #pragma unroll
-      for (int t = 0; t < KMAX; ++t) {  // order does not matter for a count
-        const int j = lane + 32 * t;
+      for (int t = 0; t < KT; ++t) {  // order does not matter for a count
+        const int j = tid + kThreads * t;
         c += (j < m) && A[j < m ? j : 0] < thr;
       }
-      const int b = __reduce_add_sync(0xffffffffu, c);
-      int bp, picks;
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) red[warp] = c;
+      __syncthreads();
+      int b = 0;
+#pragma unroll
+      for (int q = 0; q < kW; ++q) b += red[q];
+      int bp, picks, p1 = -1, base1 = 0;
       long long step;  // amount added to each picked key
       if (b == 1) {
         picks = m > 1 ? (int)min((long long)r, (A[phys(1)] - key0 + wk - 1) / wk) : r;
         bp = 1;
         step = (long long)picks * wk;
-        const int p = (int)(key0 & kWorkerMask);
-        const int base = counts[p];
-        for (int j = lane; j < picks; j += 32) worker_of[sorted[s + j]] = p + m * (base + j);
-        __syncwarp();
-        if (lane == 0) counts[p] = base + picks;
+        p1 = (int)(key0 & kWorkerMask);
+        base1 = counts[p1];
+        for (int j = tid; j < picks; j += kThreads) worker_of[sorted[s + j]] = p1 + m * (base1 + j);
       } else {
         bp = min(b, r);
         picks = bp;
         step = wk;
-        for (int j = lane; j < bp; j += 32) {
+        for (int j = tid; j < bp; j += kThreads) {  // distinct workers: no two threads share a count
           const int p = (int)(A[phys(j)] & kWorkerMask);
           const int rank = counts[p];
           counts[p] = rank + 1;
@@ -221,25 +173,62 @@ __device__ __forceinline__ void greedy_batched(const Sorted sorted, const int* b
       // merge region: new logical positions [b - bp, m) after the head moves by bp;
       // element k < bp is the re-keyed key Y_k = key(k) + step, element k >= bp the
       // tail key at logical b + (k - bp)
-      const int tail = m - b;
-      const int E = bp + tail;
-      const int iters = 32 - __clz(max(bp, tail));  // enough halvings for the larger list
+      const int E = bp + (m - b);
       const int h_new = phys(bp);
-      if (E <= 32) merge_step<1>(A, m, h, b, bp, E, step, iters, h_new);
-      else if (E <= 64 || KMAX <= 2) merge_step<(KMAX < 2 ? KMAX : 2)>(A, m, h, b, bp, E, step, iters, h_new);
-      else if (E <= 128 || KMAX <= 4) merge_step<(KMAX < 4 ? KMAX : 4)>(A, m, h, b, bp, E, step, iters, h_new);
-      else if (E <= 256 || KMAX <= 8) merge_step<(KMAX < 8 ? KMAX : 8)>(A, m, h, b, bp, E, step, iters, h_new);
-      else if (E <= 512 || KMAX <= 16) merge_step<(KMAX < 16 ? KMAX : 16)>(A, m, h, b, bp, E, step, iters, h_new);
-      else merge_step<KMAX>(A, m, h, b, bp, E, step, iters, h_new);
+      long long val[KT], tgt[KT];
+      int lo[KT], hi[KT];
+#pragma unroll
+      for (int t = 0; t < KT; ++t) {
+        const int k = tid + kThreads * t;
+        const bool live = k < E;
+        const bool is_y = k < bp;
+        int src = is_y ? k : b + k - bp;
+        src = live ? src : 0;
+        const long long a = A[phys(src)];
+        val[t] = is_y ? a + step : a;
+        tgt[t] = is_y ? val[t] : a - step;
+        lo[t] = !live ? 0 : (is_y ? b : 0);
+        hi[t] = !live ? 0 : (is_y ? m : bp);
+      }
+      const int iters = 32 - __clz(max(bp, m - b));  // enough halvings for the larger list
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int t = 0; t < KT; ++t) {
+          const int mid = (lo[t] + hi[t]) >> 1;  // lo == hi <= m still indexes the list
+          int x = h + mid;
+          x = x >= m ? x - m : x;
+          x = x >= m ? x - m : x;
+          const long long am = A[x];
+          const bool go = lo[t] < hi[t];
+          const bool less = am < tgt[t];
+          lo[t] = go && less ? mid + 1 : lo[t];
+          hi[t] = go && !less ? mid : hi[t];
+        }
+      }
+      int dst[KT];
+#pragma unroll
+      for (int t = 0; t < KT; ++t) {
+        const int k = tid + kThreads * t;
+        const int pos = k < bp ? (b - bp) + k + (lo[t] - b) : (b - bp) + (k - bp) + lo[t];
+        int x = h_new + pos;
+        x = x >= m ? x - m : x;
+        dst[t] = k < E ? x : -1;
+      }
+      __syncthreads();  // every read of the old order and of the counts is done
+#pragma unroll
+      for (int t = 0; t < KT; ++t)
+        if (dst[t] >= 0) A[dst[t]] = val[t];
+      if (tid == 0 && p1 >= 0) counts[p1] = base1 + picks;
+      __syncthreads();
       h = h_new;
       s += picks;
       r -= picks;
     }
   }
-  for (int j = lane; j < m; j += 32) final_load[A[j] & kWorkerMask] = A[j] >> kWorkerBits;
+  for (int j = tid; j < m; j += kThreads) final_load[A[j] & kWorkerMask] = A[j] >> kWorkerBits;
 }
 
-// Phase 2 with a bonus (or without staged runs): one item at a time (one warp).
+// Phase 2 with a bonus: one item at a time (one warp).
 template <int KMAX>
 __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t* __restrict__ loads,
                               const int32_t* __restrict__ home, int bonus, int n, int m, int* counts,
@@ -425,12 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   }
   __syncthreads();
 
-  // ---- phase 2: the greedy (warp 0)
-  if (tid < 32) {
-    if (counting && (home == nullptr || bonus == 0))
-      greedy_batched<KMAX>(sorted, bin_end, nbins, max_load, n, m, keys[0], counts, final_load, worker_of);
-    else
-      greedy_serial<KMAX>(sorted, loads, home, bonus, n, m, counts, final_load, worker_of);
+  // ---- phase 2: the greedy
+  if (counting && (home == nullptr || bonus == 0)) {
+    greedy_batched<(KMAX * 32 + kThreads - 1) / kThreads>(sorted, bin_end, nbins, max_load, n, m, keys[0], counts,
+                                                          final_load, worker_of, sh.scan);
+  } else if (tid < 32) {
+    greedy_serial<KMAX>(sorted, loads, home, bonus, n, m, counts, final_load, worker_of);
   }
   __syncthreads();
 
