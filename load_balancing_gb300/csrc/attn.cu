@@ -106,8 +106,7 @@ struct Cfg {
 
 struct alignas(8) Ctrl {
   uint64_t q_full[kQBufs], q_empty[kQBufs];
-  uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t k_full[kKStages];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t item_full[2], item_empty[2];
   uint64_t xbar[2], lbar[2];      // row-max (per block) and row-sum (per item) exchange
@@ -227,10 +226,12 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
     if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
     begin = end = 0;
   }
-  uint32_t item_cnt = 0, q_cnt = 0, t_cnt = 0;  // items published, Q tiles, K or V tiles issued
-  const int kstages = which == 0 ? kKStages : kVStages;
-  uint64_t* full = which == 0 ? c->k_full : c->v_full;
-  uint64_t* empty = which == 0 ? c->k_empty : c->v_empty;
+  uint32_t item_cnt = 0, q_cnt = 0, t_cnt = 0;  // items published, Q tiles, K or V tiles (= blocks) issued
+  const uint32_t kstages = which == 0 ? kKStages : kVStages;
+  // A stage is free once the product that read its previous tile has completed: S for
+  // K (s_full), PV for V (pv_done). K lands on k_full; V lands on p_full of its block,
+  // next to the softmax warps' arrivals, so the PV issuer tests a single barrier.
+  uint64_t* done = which == 0 ? c->s_full : c->pv_done;
   const uint32_t ring = smem_u32(data + (which == 0 ? C::kKOff : C::kVOff));
   const CUtensorMap* map = which == 0 ? tk : tv;
   bool ok = true;
@@ -296,10 +297,13 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
           while (wb && ok) {
             const int col = c0 + 32 * w + (__ffs(wb) - 1);
             wb &= wb - 1;
-            const uint32_t s = t_cnt % kstages, u = t_cnt / kstages;
-            ok = wait_bar(c, smem_u32(&empty[s]), (u & 1) ^ 1, p.err);
+            const uint32_t s = t_cnt % kstages;
+            if (t_cnt >= kstages) {
+              const uint32_t prev = t_cnt - kstages;
+              ok = wait_bar(c, smem_u32(&done[prev % kSBufs]), (prev / kSBufs) & 1, p.err);
+            }
             if (ok) {
-              const uint32_t f = smem_u32(&full[s]);
+              const uint32_t f = smem_u32(which == 0 ? &c->k_full[s] : &c->p_full[t_cnt % kSBufs]);
               mbar_arrive_expect_tx(f, C::kTx);
               const uint32_t dst = ring + s * C::kTileBytes;
               const int row = (int)(kv_row0 + (long long)col * BLOCK);
@@ -316,8 +320,10 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
   }
   // teardown: let every copy this warp started land before shared memory goes away
   if (lane == 0) {
-    for (uint32_t k = t_cnt > (uint32_t)kstages ? t_cnt - kstages : 0; k < t_cnt; ++k)
-      drain_bar(smem_u32(&full[k % kstages]), (k / kstages) & 1);
+    for (uint32_t k = t_cnt > kstages ? t_cnt - kstages : 0; k < t_cnt; ++k) {
+      if (which == 0) drain_bar(smem_u32(&c->k_full[k % kstages]), (k / kstages) & 1);
+      else drain_bar(smem_u32(&c->p_full[k % kSBufs]), (k / kSBufs) & 1);
+    }
     for (uint32_t k = q_cnt > (uint32_t)kQBufs ? q_cnt - kQBufs : 0; k < q_cnt; ++k)
       drain_bar(smem_u32(&c->q_full[k % kQBufs]), (k / kQBufs) & 1);
   }
@@ -360,7 +366,6 @@ __device__ void run_mma_s(const AttnParams& p, Ctrl* c, uint32_t data, uint32_t 
         const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * C::kTileChunk + (kk & 3) * 32, 16, 1024);
         mma_bf16_ss(tmem + kSCol + b * 128, a, bd, C::kIdescS, kk > 0);
       }
-      mma_commit(smem_u32(&c->k_empty[kst]));
       mma_commit(smem_u32(&c->s_full[b]));
     }
     if (!ok) break;
@@ -387,8 +392,7 @@ __device__ void run_mma_pv(const AttnParams& p, Ctrl* c, uint32_t data, uint32_t
     if (item < 0) break;
     for (int j = 0; j < n && ok; ++j, ++G, ++vs) {
       const uint32_t b = G % kSBufs, vst = vs % kVStages;
-      ok = wait_bar(c, smem_u32(&c->p_full[b]), (G / kSBufs) & 1, p.err) &&
-           wait_bar(c, smem_u32(&c->v_full[vst]), (vs / kVStages) & 1, p.err);
+      ok = wait_bar(c, smem_u32(&c->p_full[b]), (G / kSBufs) & 1, p.err);  // P(G) and V(G)
       if (!ok) break;
       tc_fence_after();
       const uint32_t vb = data + C::kVOff + vst * C::kTileBytes;
@@ -398,7 +402,6 @@ __device__ void run_mma_pv(const AttnParams& p, Ctrl* c, uint32_t data, uint32_t
         const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, C::kTileChunk, 1024);
         mma_bf16_ts(tmem, pcol + kk * 8, bd, C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       }
-      mma_commit(smem_u32(&c->v_empty[vst]));
       mma_commit(smem_u32(&c->pv_done[b]));
       ++blocks;
     }
@@ -633,17 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
       mbar_init(smem_u32(&c->q_full[i]), 1);
       mbar_init(smem_u32(&c->q_empty[i]), 1);
     }
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(smem_u32(&c->k_full[i]), 1);
-      mbar_init(smem_u32(&c->k_empty[i]), 1);
-    }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(smem_u32(&c->v_full[i]), 1);
-      mbar_init(smem_u32(&c->v_empty[i]), 1);
-    }
+    for (int i = 0; i < kKStages; ++i) mbar_init(smem_u32(&c->k_full[i]), 1);
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(smem_u32(&c->s_full[i]), 1);
-      mbar_init(smem_u32(&c->p_full[i]), 8);
+      mbar_init(smem_u32(&c->p_full[i]), 9);  // 8 softmax warps + the V producer
       mbar_init(smem_u32(&c->pv_done[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
