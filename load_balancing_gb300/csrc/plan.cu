@@ -8,7 +8,9 @@
 // choice and the worker accrues the item's true load.
 //
 // Worker keys are packed as (load << 11 | worker), so the greedy's choice (lowest
-// load, then lowest index) is the smallest int64 key. One CTA of 256 threads:
+// load, then lowest index) is the smallest key: 32-bit when every worker load stays
+// below 2^20 (LPT keeps the largest below total / m + max_load), else 64-bit. One
+// CTA of 256 threads:
 //
 //   phase 0  check loads and home, find the load range; when n <= 45056 and every
 //            load <= 4095 the loads are staged in shared memory as uint16
@@ -53,6 +55,7 @@ constexpr size_t kDynBytes = kStagedBytes > kGlobalBytes ? kStagedBytes : kGloba
 
 struct PlanShared {
   int min_load, max_load, bad_home;
+  unsigned long long total_load;
   int scan[kThreads / 32 + 1];
 };
 
@@ -108,9 +111,9 @@ struct Sorted {  // the stable order, staged in shared memory or in the worklist
 // move, and only the "tail" (keys at or above the threshold) is merged with the
 // re-keyed keys: every element is placed by a binary search in the other list, KT
 // elements per thread, all searches of a batch in parallel.
-template <int KT>
+template <int KT, typename K>
 __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbins, int max_load, int n, int m,
-                               long long* A, int* counts, long long* final_load,
+                               K* A, int* counts, long long* final_load,
                                int32_t* __restrict__ worker_of, int* red) {
   constexpr int kW = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -125,7 +128,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
     if (r <= 0) continue;
     const int w = max_load - bin;
     if (w == 0) {  // zero loads never change a key: they all go to the current minimum
-      const int p0 = (int)(A[h] & kWorkerMask);
+      const int p0 = (int)(A[h] & (K)kWorkerMask);
       const int base = counts[p0];
       for (int j = tid; j < r; j += kThreads) worker_of[sorted[s + j]] = p0 + m * (base + j);
       __syncthreads();
@@ -134,10 +137,10 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
       s = e;
       continue;
     }
-    const long long wk = (long long)w << kWorkerBits;
+    const K wk = (K)w << kWorkerBits;
     while (r > 0) {
-      const long long key0 = A[h];
-      const long long thr = key0 + wk;
+      const K key0 = A[h];
+      const K thr = key0 + wk;
       int c = 0;
 #pragma unroll
       for (int t = 0; t < KT; ++t) {  // order does not matter for a count
@@ -151,12 +154,12 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
 #pragma unroll
       for (int q = 0; q < kW; ++q) b += red[q];
       int bp, picks, p1 = -1, base1 = 0;
-      long long step;  // amount added to each picked key
+      K step;  // amount added to each picked key
       if (b == 1) {
-        picks = m > 1 ? (int)min((long long)r, (A[phys(1)] - key0 + wk - 1) / wk) : r;
+        picks = m > 1 ? (int)min((long long)r, (long long)((A[phys(1)] - key0 + wk - 1) / wk)) : r;
         bp = 1;
-        step = (long long)picks * wk;
-        p1 = (int)(key0 & kWorkerMask);
+        step = (K)picks * wk;
+        p1 = (int)(key0 & (K)kWorkerMask);
         base1 = counts[p1];
         for (int j = tid; j < picks; j += kThreads) worker_of[sorted[s + j]] = p1 + m * (base1 + j);
       } else {
@@ -164,7 +167,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
         picks = bp;
         step = wk;
         for (int j = tid; j < bp; j += kThreads) {  // distinct workers: no two threads share a count
-          const int p = (int)(A[phys(j)] & kWorkerMask);
+          const int p = (int)(A[phys(j)] & (K)kWorkerMask);
           const int rank = counts[p];
           counts[p] = rank + 1;
           worker_of[sorted[s + j]] = p + m * rank;
@@ -175,8 +178,8 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
       // tail key at logical b + (k - bp)
       const int E = bp + (m - b);
       const int h_new = phys(bp);
-      long long val[KT], tgt[KT];
-      int lo[KT], hi[KT];
+      K val[KT], add[KT];
+      int lo[KT], hi[KT], depth[KT];
 #pragma unroll
       for (int t = 0; t < KT; ++t) {
         const int k = tid + kThreads * t;
@@ -184,13 +187,16 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
         const bool is_y = k < bp;
         int src = is_y ? k : b + k - bp;
         src = live ? src : 0;
-        const long long a = A[phys(src)];
+        const K a = A[phys(src)];
         val[t] = is_y ? a + step : a;
-        tgt[t] = is_y ? val[t] : a - step;
+        add[t] = is_y ? (K)0 : step;  // a tail key is compared with re-keyed keys: add the step
         lo[t] = !live ? 0 : (is_y ? b : 0);
         hi[t] = !live ? 0 : (is_y ? m : bp);
+        depth[t] = 32 - __clz(hi[t] - lo[t]);  // halvings for the list searched
       }
-      const int iters = 32 - __clz(max(bp, m - b));  // enough halvings for the larger list
+      int iters = 0;
+#pragma unroll
+      for (int t = 0; t < KT; ++t) iters = max(iters, depth[t]);
       for (int it = 0; it < iters; ++it) {
 #pragma unroll
         for (int t = 0; t < KT; ++t) {
@@ -198,9 +204,9 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
           int x = h + mid;
           x = x >= m ? x - m : x;
           x = x >= m ? x - m : x;
-          const long long am = A[x];
+          const K am = A[x] + add[t];
           const bool go = lo[t] < hi[t];
-          const bool less = am < tgt[t];
+          const bool less = am < val[t];
           lo[t] = go && less ? mid + 1 : lo[t];
           hi[t] = go && !less ? mid : hi[t];
         }
@@ -225,7 +231,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
       r -= picks;
     }
   }
-  for (int j = tid; j < m; j += kThreads) final_load[A[j] & kWorkerMask] = A[j] >> kWorkerBits;
+  for (int j = tid; j < m; j += kThreads) final_load[A[j] & (K)kWorkerMask] = (long long)(A[j] >> kWorkerBits);
 }
 
 // Phase 2 with a bonus: one item at a time (one warp).
@@ -305,14 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   const int tid = threadIdx.x, lane = tid & 31;
 
   // ---- phase 0: validate and find the load range
-  if (tid == 0) { sh.min_load = INT_MAX; sh.max_load = INT_MIN; sh.bad_home = 0; }
+  if (tid == 0) { sh.min_load = INT_MAX; sh.max_load = INT_MIN; sh.bad_home = 0; sh.total_load = 0; }
   __syncthreads();
   int lmin = INT_MAX, lmax = INT_MIN, badh = 0;
+  unsigned long long tot = 0;
   for (int i = tid; i < n; i += kThreads) {
     const int w = loads[i];
     lmin = min(lmin, w); lmax = max(lmax, w);
+    tot += (unsigned long long)max(w, 0);
     if (home) { const int h = home[i]; badh |= (h < 0 || h >= m); }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane == 0) atomicAdd(&sh.total_load, tot);  // one atomic per warp
   atomicMin(&sh.min_load, lmin);
   atomicMax(&sh.max_load, lmax);
   if (badh) atomicOr(&sh.bad_home, 1);
@@ -416,8 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
 
   // ---- phase 2: the greedy
   if (counting && (home == nullptr || bonus == 0)) {
-    greedy_batched<(KMAX * 32 + kThreads - 1) / kThreads>(sorted, bin_end, nbins, max_load, n, m, keys[0], counts,
-                                                          final_load, worker_of, sh.scan);
+    // LPT keeps every worker within max_load of the average, so the final worker load is
+    // below total / m + max_load; 32-bit keys (load < 2^21) halve the shared-memory
+    // traffic of the batch merges whenever that bound allows
+    constexpr int KT = (KMAX * 32 + kThreads - 1) / kThreads;
+    const bool key32 = sh.total_load / (unsigned long long)m + (unsigned long long)max_load < (1ull << 20);
+    if (key32)
+      greedy_batched<KT, uint32_t>(sorted, bin_end, nbins, max_load, n, m, reinterpret_cast<uint32_t*>(keys[0]),
+                                   counts, final_load, worker_of, sh.scan);
+    else
+      greedy_batched<KT, long long>(sorted, bin_end, nbins, max_load, n, m, keys[0], counts, final_load,
+                                    worker_of, sh.scan);
   } else if (tid < 32) {
     greedy_serial<KMAX>(sorted, loads, home, bonus, n, m, counts, final_load, worker_of);
   }

@@ -114,3 +114,16 @@ def test_bad_inputs_set_device_status(built_library, cuda_device):
     assert got["status"] == 2
     # the error word is cleared by the read: a good call afterwards is clean
     _assert_same(_plan([1, 2, 3], 2), OP.lpt_plan([1, 2, 3], 2))
+
+
+@pytest.mark.parametrize("m,lo,hi", [(64, 1800, 2048), (300, 20000, 32768)])
+def test_key_width_boundary(built_library, cuda_device, m, lo, hi):
+    """Worker keys are 32-bit while total / m + max_load < 2^20 and 64-bit beyond;
+    instances on both sides of that bound give the textbook LPT."""
+    rng = np.random.default_rng(m)
+    mean = (lo + hi - 1) / 2
+    for target in ((1 << 20) * 0.97, (1 << 20) * 1.03):
+        n = int((target - (hi - 1)) * m / mean)
+        loads = rng.integers(lo, hi, n)
+        loads[0] = hi - 1
+        _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
