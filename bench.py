@@ -507,15 +507,34 @@ def run_suite(args):
                                    "frac_of_bf16_peak": flop / t / 1e9 / float(peaks["bf16_tflops"]),
                                    "sm_skew": float((busy.max() - busy.mean()) / busy.mean()),
                                    "blocks_max_over_mean": float(tt[:, 2].max() / max(1e-9, tt[:, 2].mean()))}
-        # a5: merge of KV-shard partials (sharded workload)
+        # head-level LPT over a few "virtual GPUs" (db-SP blog, scenario 1): makespan
+        # against the lower bound max(ceil(total / m), largest head)
+        hl = pb.head_loads.view(-1).contiguous()
+        total, largest = int(hl.sum().item()), int(hl.max().item())
+        line["head_lpt"] = {}
+        for mv in (2, 4, 8):
+            hp = P.alloc_plan(1, 1, hl.numel(), 1, mv, dev)
+            dbsp.dbsp_plan_lpt(hl, mv, hp.worker_of, hp.worker_offsets, hp.worklist, hp.worker_loads, stream=stream)
+            makespan = int(hp.worker_loads.max().item())
+            bound = max(-(-total // mv), largest)
+            line["head_lpt"][str(mv)] = {"makespan": makespan, "lower_bound": bound, "ratio": makespan / bound}
+        # a5: merge of KV-shard partials (sharded workload), shards contiguous, striped
+        # or planned by LPT over the KV blocks' column loads (db-SP blog, scenario 2)
         if "n_shards" in w.extra:
             n_sh = w.extra["n_shards"]
-            for layout in ("contiguous", "striped"):
-                shards = torch.from_numpy(W.shard_masks(mask_np, n_sh, layout)).to(dev)
+            for layout in ("contiguous", "striped", "lpt"):
+                if layout == "lpt":
+                    sp = P.plan_kv_shards(mask, n_sh, stream=stream)
+                    t_sp = _time_ms(lambda: P.plan_kv_shards(mask, n_sh, stream=stream), stream, flush, reps)
+                    shards = P.shard_masks_from_plan(mask, sp)
+                else:
+                    t_sp = None
+                    shards = torch.from_numpy(W.shard_masks(mask_np, n_sh, layout)).to(dev)
                 o_p = torch.empty((n_sh, w.B, w.H, w.S, w.d), dtype=torch.float32, device=dev)
                 m_p = torch.empty((n_sh, w.B, w.H, w.S), dtype=torch.float32, device=dev)
                 l_p = torch.empty_like(m_p)
-                plans = [P.plan(shards[s], m) for s in range(n_sh)]
+                plans = [P.plan(shards[s], m, block_cost=P.SHARD_BLOCK_COST, item_cost=P.SHARD_ITEM_COST)
+                         for s in range(n_sh)]
 
                 def partials():
                     for s in range(n_sh):
@@ -528,11 +547,18 @@ def run_suite(args):
                                                          stream=stream)
                 t = _time_ms(merge, stream, flush, reps)
                 rows = w.B * w.H * w.S
-                nbytes = n_sh * rows * (4 * w.d + 8) + rows * (2 * w.d + 4)
+                # an empty partial's O is never read: count the live ones
+                live = int(((l_p > 0) & torch.isfinite(m_p)).sum().item())
+                nbytes = live * 4 * w.d + n_sh * rows * 8 + rows * (2 * w.d + 4)
+                shard_load = np.array([int(pl.head_loads.sum().item()) for pl in plans], dtype=np.float64)
                 line[f"merge_{layout}"] = {"us": 1e3 * t, "GB/s": nbytes / t / 1e6, "bytes": nbytes,
                                            "frac_of_hbm": nbytes / t / 1e6 / float(peaks["hbm_gbs"]),
                                            "partials_us": 1e3 * t_part,
-                                           "partials_TFLOP/s": flop / t_part / 1e9}
+                                           "partials_TFLOP/s": flop / t_part / 1e9,
+                                           "shard_loads": shard_load.astype(int).tolist(),
+                                           "shard_max_over_mean": float(shard_load.max() / shard_load.mean())}
+                if t_sp is not None:
+                    line[f"merge_{layout}"]["shard_plan_us"] = 1e3 * t_sp
         line["peaks"] = {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
         status = dbsp.dbsp_device_status()
         line["device_status"] = status

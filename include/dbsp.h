@@ -77,6 +77,22 @@ DBSP_API int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, in
                           void* stream);
 
 /*
+ * KV-block loads across heads.  [db-SP blog, scenario 2]: a KV-block's load is the
+ * number of dense blocks in its mask column; when the KV sequence is split into
+ * shards shared by every head (sequence parallelism), the load that a shard
+ * receives from block j is the column count summed over all heads.
+ *
+ *   col_loads   int32 [groups, nK]  column loads, e.g. dbsp_block_mask_loads's
+ *               col_loads with groups = B * H.
+ *   kv_loads    int32 [nK]  out: kv_loads[j] = sum over g of col_loads[g, j].
+ * Requires groups, nK >= 1 and groups * nK < 2^31. Exact; one kernel launch. The
+ * result can be planned over shards with dbsp_plan_lpt (items = KV blocks,
+ * workers = shards).
+ */
+DBSP_API int dbsp_kv_block_loads(const int32_t* col_loads, int groups, int nK, int32_t* kv_loads,
+                                 void* stream);
+
+/*
  * LPT plan with stay-in-place bonus.  [db-SP blog, scenario 1]: repeatedly give
  * the largest remaining item to the currently least-loaded worker (LPT).
  * [db-SP blog, scenario 2, third bullet]: an item placed on its original worker
@@ -103,6 +119,23 @@ DBSP_API int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, in
 DBSP_API int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
                   int32_t stay_bonus, int32_t* worker_of, int32_t* worker_offsets,
                   int32_t* worklist, int64_t* worker_loads, void* stream);
+
+/*
+ * LPT plan over planning loads loads[i] * block_cost + item_cost.  The pages count
+ * work in dense blocks ([db-SP blog, scenario 2, first bullet]), which is
+ * dbsp_plan_lpt (block_cost = 1, item_cost = 0). On one GPU an item also costs
+ * something of its own (its Q tile, its epilogue): with item_cost > 0 items without
+ * dense blocks no longer all land on the least-loaded worker. The transform keeps
+ * the order of the items (block_cost >= 1), so only the worker choice changes.
+ *
+ *   block_cost in [1, 65535], item_cost in [0, 2^24]; every other argument as in
+ *   dbsp_plan_lpt, and worker_loads accrues the planning loads. A planning load of
+ *   2^31 or more sets DBSP_ERR_UNSUPPORTED on the device.
+ */
+DBSP_API int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
+                       int32_t stay_bonus, int32_t block_cost, int32_t item_cost,
+                       int32_t* worker_of, int32_t* worker_offsets, int32_t* worklist,
+                       int64_t* worker_loads, void* stream);
 
 /*
  * Block-sparse attention forward over an LPT worklist.  [6D notes §2.1, step 2]:

@@ -15,7 +15,8 @@
 // 12 warps:
 //   warp 0      producer of Q and K: reads each item's mask row 16 bytes per lane,
 //               publishes (id, dense count), TMA-loads the Q tile (two buffers) and
-//               the dense K tiles into a ring;
+//               the dense K tiles into a ring; an item without dense blocks is not
+//               published: this warp writes its output rows itself;
 //   warp 1      producer of V: walks the same items and loads the dense V tiles into
 //               a second ring (S runs ahead of PV, so K and V are consumed at
 //               different times);
@@ -251,6 +252,24 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
       limit = rs.limit(item);
       if (which == 0)
         for (int c0 = 0; c0 < limit; c0 += 512) n += __reduce_add_sync(kAll, __popc(rs.bits(item, c0, limit)));
+    }
+    if (which == 0 && item >= 0 && n == 0) {
+      // An item without dense blocks never reaches the MMA issuers or the softmax: this
+      // warp writes its rows itself (partial mode: m = -inf, l = 0, O rows untouched;
+      // final mode: O = 0, LSE = -inf).
+      const long long row0 = (long long)(item / p.nQ) * p.S + (long long)(item % p.nQ) * BLOCK;
+      if (p.o_part) {
+        for (int r = lane; r < BLOCK; r += 32) {
+          p.m_part[row0 + r] = -INFINITY;
+          p.l_part[row0 + r] = 0.f;
+        }
+      } else {
+        uint4* o = reinterpret_cast<uint4*>(p.out + row0 * D);
+        for (int i = lane; i < BLOCK * D / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse)
+          for (int r = lane; r < BLOCK; r += 32) p.lse[row0 + r] = -INFINITY;
+      }
+      continue;
     }
     if (which == 0) {  // publish the item
       const int diag = item >= 0 && p.causal && p.mask[(long long)item * p.nK + item % p.nQ] != 0;

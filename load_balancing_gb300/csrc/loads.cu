@@ -66,20 +66,40 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
   if (r_off < r_step) {
     for (int c = c0; c < cpr; c += c_step) {
       if (VEC == 16) {
-        // per-byte column counters: 4 words of byte-wide counters, flushed every 255 rows
+        // per-byte column counters: 4 words of byte-wide counters, flushed every 252 rows;
+        // kUnroll rows are loaded before any is counted, so that many loads are in flight
+        constexpr int kUnroll = 4;
         int cols[16];
 #pragma unroll
         for (int b = 0; b < 16; ++b) cols[b] = 0;
         uint32_t acc[4] = {0, 0, 0, 0};
         int pending = 0;
-        for (int r = row0 + r_off; r < row1; r += r_step) {
-          const uint4 x = __ldg(reinterpret_cast<const uint4*>(head_mask + (long long)r * nK) + c);
-          const uint32_t f0 = nonzero_byte_flags(x.x), f1 = nonzero_byte_flags(x.y);
-          const uint32_t f2 = nonzero_byte_flags(x.z), f3 = nonzero_byte_flags(x.w);
-          acc[0] += f0; acc[1] += f1; acc[2] += f2; acc[3] += f3;
-          const int cnt = __popc(f0) + __popc(f1) + __popc(f2) + __popc(f3);
-          if (cnt) atomicAdd(&row_acc[r - row0], cnt);
-          if (++pending == 255) {
+        // a warp that covers 32 units of one row adds its row count once
+        const bool warp_row = cpr >= 32 && (cpr % 32) == 0;
+        for (int r = row0 + r_off; r < row1; r += kUnroll * r_step) {
+          uint4 x[kUnroll];
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int ru = r + u * r_step;
+            x[u] = ru < row1 ? __ldg(reinterpret_cast<const uint4*>(head_mask + (long long)ru * nK) + c)
+                             : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int ru = r + u * r_step;
+            const uint32_t f0 = nonzero_byte_flags(x[u].x), f1 = nonzero_byte_flags(x[u].y);
+            const uint32_t f2 = nonzero_byte_flags(x[u].z), f3 = nonzero_byte_flags(x[u].w);
+            acc[0] += f0; acc[1] += f1; acc[2] += f2; acc[3] += f3;
+            int cnt = __popc(f0) + __popc(f1) + __popc(f2) + __popc(f3);
+            if (warp_row) {
+              cnt = __reduce_add_sync(__activemask(), cnt);
+              if ((tid & 31) == 0 && cnt && ru < row1) atomicAdd(&row_acc[ru - row0], cnt);
+            } else if (cnt) {
+              atomicAdd(&row_acc[ru - row0], cnt);
+            }
+          }
+          pending += kUnroll;
+          if (pending >= 252) {
 #pragma unroll
             for (int b = 0; b < 16; ++b) cols[b] += (acc[b >> 2] >> (8 * (b & 3))) & 0xff;
             acc[0] = acc[1] = acc[2] = acc[3] = 0;
@@ -129,7 +149,32 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
   cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
+// KV-block loads summed over (b, h): thread j adds column j of every head.
+__global__ void __launch_bounds__(kThreads) kv_block_loads_kernel(const int32_t* __restrict__ col_loads,
+                                                                  int groups, int nK,
+                                                                  int32_t* __restrict__ kv_loads) {
+  const int j = blockIdx.x * kThreads + threadIdx.x;
+  if (j >= nK) return;
+  int s = 0;
+  for (int g = 0; g < groups; ++g) s += __ldg(col_loads + (long long)g * nK + j);
+  kv_loads[j] = s;
+}
+
 }  // namespace
+
+extern "C" int dbsp_kv_block_loads(const int32_t* col_loads, int groups, int nK, int32_t* kv_loads,
+                                   void* stream) {
+  if (!col_loads || !kv_loads || groups < 1 || nK < 1) return DBSP_ERR_INVALID_ARG;
+  if ((long long)groups * nK >= (1LL << 31)) return DBSP_ERR_INVALID_ARG;
+  if (!dbsp::aligned(col_loads, 4) || !dbsp::aligned(kv_loads, 4)) return DBSP_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = dbsp::check_device(&dev);
+  if (st != DBSP_OK) return st;
+  kv_block_loads_kernel<<<(nK + kThreads - 1) / kThreads, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      col_loads, groups, nK, kv_loads);
+  DBSP_LAUNCH_CHECK("launch kv_block_loads");
+  return DBSP_OK;
+}
 
 extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK,
                                      int32_t* row_loads, int32_t* col_loads,

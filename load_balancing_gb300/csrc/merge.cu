@@ -9,9 +9,9 @@
 // A partial with l_k == 0 or m_k == -inf is empty and contributes nothing.
 //
 // Layout: o_parts [n_shards, rows, d] fp32, m/l [n_shards, rows] fp32. One thread
-// owns 4 consecutive elements of a row (float4 loads, streaming cache hint,
-// coalesced along d) and writes 4 bf16 (one 8-byte store). HBM-bound: each
-// partial is read exactly once.
+// owns four float4 groups of a row, strided so that each load instruction of a warp
+// reads contiguous 128-byte runs (streaming cache hint), and writes them as bf16
+// (8-byte stores); the shard weights are computed once per thread for its 16 elements. HBM-bound: each live partial is read exactly once.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -22,17 +22,19 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kChunk = 8;  // shards whose loads are in flight together
+constexpr int kQuads = 4;  // float4 groups of one row per thread (16 consecutive elements)
 
 __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
     const float* __restrict__ o_parts, const float* __restrict__ m_parts,
     const float* __restrict__ l_parts, int n_shards, long long rows, int d,
     __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   const int quads = d >> 2;
-  const long long total = rows * quads;
+  const int groups = (quads + kQuads - 1) / kQuads;  // threads per row
+  const long long total = rows * groups;
   const long long stride = (long long)gridDim.x * kThreads;
   for (long long u = (long long)blockIdx.x * kThreads + threadIdx.x; u < total; u += stride) {
-    const long long row = u / quads;
-    const int c4 = (int)(u - row * quads);
+    const long long row = u / groups;
+    const int qt = (int)(u - row * groups);  // this thread's float4s: qt, qt + groups, ... (coalesced)
     // pass 1: m* over live partials
     float mstar = -INFINITY;
     for (int k = 0; k < n_shards; ++k) {
@@ -40,12 +42,14 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
       const float lk = __ldg(l_parts + (long long)k * rows + row);
       if (lk > 0.f && mk > -INFINITY) mstar = fmaxf(mstar, mk);
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[kQuads];
+#pragma unroll
+    for (int i = 0; i < kQuads; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
     if (mstar > -INFINITY) {
-      // pass 2, kChunk shards at a time: the weights first, then the chunk's
-      // partial loads as independent predicated streams (no load waits on
-      // another), then the weighted sums.
+      // pass 2, kChunk shards at a time: the weights first, then the chunk's partial
+      // loads as independent predicated streams (an empty partial is never read),
+      // then the weighted sums
       for (int k0 = 0; k0 < n_shards; k0 += kChunk) {
         float w[kChunk];
 #pragma unroll
@@ -61,28 +65,38 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
             }
           }
         }
-        float4 o[kChunk];
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (w[j] > 0.f)
-            o[j] = __ldcs(reinterpret_cast<const float4*>(o_parts + ((long long)(k0 + j) * rows + row) * d) + c4);
-        }
+          if (w[j] > 0.f) {
+            const float4* src = reinterpret_cast<const float4*>(o_parts + ((long long)(k0 + j) * rows + row) * d) + qt;
+            float4 o[kQuads];
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          acc.x += w[j] * o[j].x; acc.y += w[j] * o[j].y; acc.z += w[j] * o[j].z; acc.w += w[j] * o[j].w;
+            for (int i = 0; i < kQuads; ++i)
+              o[i] = qt + i * groups < quads ? __ldcs(src + i * groups) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kQuads; ++i) {
+              acc[i].x += w[j] * o[i].x; acc[i].y += w[j] * o[i].y;
+              acc[i].z += w[j] * o[i].z; acc[i].w += w[j] * o[i].w;
+            }
+          }
         }
       }
       const float inv = 1.f / l;
-      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+#pragma unroll
+      for (int i = 0; i < kQuads; ++i) { acc[i].x *= inv; acc[i].y *= inv; acc[i].z *= inv; acc[i].w *= inv; }
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    __stcs(reinterpret_cast<uint2*>(out + row * d) + c4, packed);
-    if (lse && c4 == 0) lse[row] = mstar > -INFINITY ? mstar + logf(l) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kQuads; ++i) {
+      if (qt + i * groups < quads) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x, acc[i].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z, acc[i].w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        __stcs(reinterpret_cast<uint2*>(out + row * d) + qt + i * groups, packed);
+      }
+    }
+    if (lse && qt == 0) lse[row] = mstar > -INFINITY ? mstar + logf(l) : -INFINITY;
   }
 }
 
@@ -101,7 +115,7 @@ extern "C" int dbsp_merge_partials(const float* o_parts, const float* m_parts, c
   int dev = 0;
   int st = dbsp::check_device(&dev);
   if (st != DBSP_OK) return st;
-  const long long units = rows * (d / 4);
+  const long long units = rows * ((d / 4 + kQuads - 1) / kQuads);
   const long long want = (units + kThreads - 1) / kThreads;
   const int blocks = (int)std::min<long long>(want, (long long)dbsp::sm_count(dev) * 8);
   merge_partials_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(

@@ -113,7 +113,7 @@ struct Sorted {  // the stable order, staged in shared memory or in the worklist
 // elements per thread, all searches of a batch in parallel.
 template <int KT, typename K>
 __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbins, int max_load, int n, int m,
-                               K* A, int* counts, long long* final_load,
+                               int bc, int ic, K* A, int* counts, long long* final_load,
                                int32_t* __restrict__ worker_of, int* red) {
   constexpr int kW = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -126,7 +126,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
     const int e = bin_end[bin];
     int r = e - s;
     if (r <= 0) continue;
-    const int w = max_load - bin;
+    const int w = (max_load - bin) * bc + ic;  // the planning load of this run's items
     if (w == 0) {  // zero loads never change a key: they all go to the current minimum
       const int p0 = (int)(A[h] & (K)kWorkerMask);
       const int base = counts[p0];
@@ -237,7 +237,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
 // Phase 2 with a bonus: one item at a time (one warp).
 template <int KMAX>
 __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t* __restrict__ loads,
-                              const int32_t* __restrict__ home, int bonus, int n, int m, int* counts,
+                              const int32_t* __restrict__ home, int bonus, int bc, int ic, int n, int m, int* counts,
                               long long* final_load, int32_t* __restrict__ worker_of) {
   const int lane = threadIdx.x & 31;
   long long key[KMAX];
@@ -255,7 +255,7 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
     int my_i = 0, my_w = 0, my_h = -1;
     if (t < n) {
       my_i = sorted[t];
-      my_w = loads[my_i];
+      my_w = loads[my_i] * bc + ic;
       if (home) my_h = home[my_i];
     }
     const int chunk = min(32, n - base);
@@ -301,7 +301,7 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     const int32_t* __restrict__ loads, const int32_t* __restrict__ home, int n, int m,
-    int bonus, int32_t* __restrict__ worker_of, int32_t* __restrict__ offsets,
+    int bonus, int bc, int ic, int32_t* __restrict__ worker_of, int32_t* __restrict__ offsets,
     int32_t* __restrict__ worklist, int64_t* __restrict__ worker_loads, int* err) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ PlanShared sh;
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   for (int i = tid; i < n; i += kThreads) {
     const int w = loads[i];
     lmin = min(lmin, w); lmax = max(lmax, w);
-    tot += (unsigned long long)max(w, 0);
+    tot += (unsigned long long)max(w, 0) * (unsigned long long)bc + (unsigned long long)ic;
     if (home) { const int h = home[i]; badh |= (h < 0 || h >= m); }
   }
 #pragma unroll
@@ -330,9 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   __syncthreads();
   const bool ok_vals = n == 0 || (sh.min_load >= 0 && !sh.bad_home);
   const int max_load = n ? sh.max_load : 0;
+  // planning loads load * bc + ic must stay within int
+  const bool ok_cost = (long long)max_load * bc + ic < (1LL << 31);
   const bool staged = n <= kStagedMaxItems && max_load <= kStagedMaxLoad;
   const bool counting = max_load <= kMaxLoadCounting;
-  if (!ok_vals || (!counting && n > kMaxItemsCompare)) {
+  if (!ok_vals || !ok_cost || (!counting && n > kMaxItemsCompare)) {
     if (tid == 0) dbsp::report(err, ok_vals ? DBSP_ERR_UNSUPPORTED : DBSP_ERR_INVALID_ARG);
     for (int p = tid; p <= m; p += kThreads) offsets[p] = 0;
     return;
@@ -431,15 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     // below total / m + max_load; 32-bit keys (load < 2^21) halve the shared-memory
     // traffic of the batch merges whenever that bound allows
     constexpr int KT = (KMAX * 32 + kThreads - 1) / kThreads;
-    const bool key32 = sh.total_load / (unsigned long long)m + (unsigned long long)max_load < (1ull << 20);
+    const bool key32 = sh.total_load / (unsigned long long)m + (unsigned long long)max_load * bc + ic < (1ull << 20);
     if (key32)
-      greedy_batched<KT, uint32_t>(sorted, bin_end, nbins, max_load, n, m, reinterpret_cast<uint32_t*>(keys[0]),
-                                   counts, final_load, worker_of, sh.scan);
+      greedy_batched<KT, uint32_t>(sorted, bin_end, nbins, max_load, n, m, bc, ic,
+                                   reinterpret_cast<uint32_t*>(keys[0]), counts, final_load, worker_of, sh.scan);
     else
-      greedy_batched<KT, long long>(sorted, bin_end, nbins, max_load, n, m, keys[0], counts, final_load,
+      greedy_batched<KT, long long>(sorted, bin_end, nbins, max_load, n, m, bc, ic, keys[0], counts, final_load,
                                     worker_of, sh.scan);
   } else if (tid < 32) {
-    greedy_serial<KMAX>(sorted, loads, home, bonus, n, m, counts, final_load, worker_of);
+    greedy_serial<KMAX>(sorted, loads, home, bonus, bc, ic, n, m, counts, final_load, worker_of);
   }
   __syncthreads();
 
@@ -459,24 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
 }
 
 template <int KMAX>
-int launch(const int32_t* loads, const int32_t* home, int n, int m, int bonus, int32_t* worker_of,
+int launch(const int32_t* loads, const int32_t* home, int n, int m, int bonus, int bc, int ic, int32_t* worker_of,
            int32_t* offsets, int32_t* worklist, int64_t* worker_loads, int* err, cudaStream_t s) {
   auto kernel = lpt_plan_kernel<KMAX>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(lpt_plan)");
-  kernel<<<1, kThreads, kDynBytes, s>>>(loads, home, n, m, bonus, worker_of, offsets, worklist, worker_loads,
-                                        err);
+  kernel<<<1, kThreads, kDynBytes, s>>>(loads, home, n, m, bonus, bc, ic, worker_of, offsets, worklist,
+                                        worker_loads, err);
   DBSP_LAUNCH_CHECK("launch lpt_plan");
   return DBSP_OK;
 }
 
 }  // namespace
 
-extern "C" int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
-                             int32_t stay_bonus, int32_t* worker_of, int32_t* worker_offsets,
-                             int32_t* worklist, int64_t* worker_loads, void* stream) {
+extern "C" int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
+                                  int32_t stay_bonus, int32_t block_cost, int32_t item_cost, int32_t* worker_of,
+                                  int32_t* worker_offsets, int32_t* worklist, int64_t* worker_loads,
+                                  void* stream) {
   if (n_items < 0 || n_workers < 1 || n_workers > DBSP_MAX_WORKERS || stay_bonus < 0)
     return DBSP_ERR_INVALID_ARG;
+  if (block_cost < 1 || block_cost > 65535 || item_cost < 0 || item_cost > (1 << 24)) return DBSP_ERR_INVALID_ARG;
   if ((long long)n_items * n_workers >= (1LL << 31)) return DBSP_ERR_INVALID_ARG;
   if (!worker_offsets) return DBSP_ERR_INVALID_ARG;
   if (n_items > 0 && (!loads || !worker_of || !worklist)) return DBSP_ERR_INVALID_ARG;
@@ -486,8 +490,9 @@ extern "C" int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_it
   int* err = dbsp::error_word(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int m = n_workers;
-#define DBSP_PLAN_CASE(K) \
-  return launch<K>(loads, home, n_items, m, stay_bonus, worker_of, worker_offsets, worklist, worker_loads, err, s)
+#define DBSP_PLAN_CASE(K)                                                                                 \
+  return launch<K>(loads, home, n_items, m, stay_bonus, block_cost, item_cost, worker_of, worker_offsets, \
+                   worklist, worker_loads, err, s)
   if (m <= 32) DBSP_PLAN_CASE(1);
   if (m <= 64) DBSP_PLAN_CASE(2);
   if (m <= 128) DBSP_PLAN_CASE(4);
@@ -495,4 +500,11 @@ extern "C" int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_it
   if (m <= 512) DBSP_PLAN_CASE(16);
   DBSP_PLAN_CASE(32);
 #undef DBSP_PLAN_CASE
+}
+
+extern "C" int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
+                             int32_t stay_bonus, int32_t* worker_of, int32_t* worker_offsets,
+                             int32_t* worklist, int64_t* worker_loads, void* stream) {
+  return dbsp_plan_lpt_cost(loads, home, n_items, n_workers, stay_bonus, 1, 0, worker_of, worker_offsets,
+                            worklist, worker_loads, stream);
 }

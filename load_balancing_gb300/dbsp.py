@@ -30,7 +30,10 @@ _SIGNATURES = {
     "dbsp_status_string": (ctypes.c_char_p, [_i32]),
     "dbsp_last_error_string": (ctypes.c_char_p, []),
     "dbsp_block_mask_loads": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "dbsp_kv_block_loads": (_i32, [_vp, _i32, _i32, _vp, _vp]),
     "dbsp_plan_lpt": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
+    "dbsp_plan_lpt_cost": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp,
+                                  _vp, _vp, _vp]),
     "dbsp_block_sparse_attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]),
@@ -103,6 +106,15 @@ def dbsp_block_mask_loads(mask, row_loads, col_loads, head_loads=None, stream=No
     _check(st, "dbsp_block_mask_loads")
 
 
+def dbsp_kv_block_loads(col_loads, kv_loads, stream=None):
+    """col_loads int32 [..., nK] (every leading dim a group) -> kv_loads int32 [nK], summed over groups."""
+    nK = col_loads.shape[-1]
+    groups = col_loads.numel() // nK
+    st = library().dbsp_kv_block_loads(_ptr(col_loads, torch.int32, "col_loads"), groups, nK,
+                                       _ptr(kv_loads, torch.int32, "kv_loads"), _stream(stream))
+    _check(st, "dbsp_kv_block_loads")
+
+
 def dbsp_plan_lpt(loads, n_workers, worker_of, worker_offsets, worklist, worker_loads=None,
                   home=None, stay_bonus=0, stream=None):
     """LPT plan: loads int32 [n] -> worker_of [n], worker_offsets [m+1], worklist [n], worker_loads int64 [m]."""
@@ -113,6 +125,18 @@ def dbsp_plan_lpt(loads, n_workers, worker_of, worker_offsets, worklist, worker_
         _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
         _ptr(worker_loads, torch.int64, "worker_loads", True), _stream(stream))
     _check(st, "dbsp_plan_lpt")
+
+
+def dbsp_plan_lpt_cost(loads, n_workers, block_cost, item_cost, worker_of, worker_offsets, worklist,
+                       worker_loads=None, home=None, stay_bonus=0, stream=None):
+    """LPT plan over planning loads ``loads * block_cost + item_cost`` (same outputs as dbsp_plan_lpt)."""
+    n = loads.numel()
+    st = library().dbsp_plan_lpt_cost(
+        _ptr(loads, torch.int32, "loads"), _ptr(home, torch.int32, "home", True), n, n_workers,
+        int(stay_bonus), int(block_cost), int(item_cost), _ptr(worker_of, torch.int32, "worker_of"),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        _ptr(worker_loads, torch.int64, "worker_loads", True), _stream(stream))
+    _check(st, "dbsp_plan_lpt_cost")
 
 
 def dbsp_block_sparse_attn_fwd(q, k, v, mask, block, causal, worker_offsets, worklist, n_workers,

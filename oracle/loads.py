@@ -7,6 +7,10 @@ in its row, the work of a KV-block the number of dense blocks in its column.
 db-SP blog, scenario 1: the work of a whole head (the item that head-level
 balancing moves between machines) is the number of dense blocks of the head.
 
+db-SP blog, scenario 2: when the KV sequence is split into shards that every head
+shares, the load a KV-block brings to its shard is its column count summed over all
+heads (``kv_block_loads``).
+
 Two versions are kept: ``block_mask_loads_loops`` walks every entry with Python
 loops (tiny masks only) and ``block_mask_loads`` uses numpy sums over ``mask != 0``.
 The tests cross-check them on mid-sized masks.
@@ -48,3 +52,14 @@ def block_mask_loads(mask):
     col = dense.sum(axis=2, dtype=np.int64)
     head = dense.sum(axis=(2, 3), dtype=np.int64)
     return row, col, head
+
+
+def kv_block_loads(mask):
+    """Column loads summed over (b, h): int64 [nK], by explicit loops over heads."""
+    _, col, _ = block_mask_loads(mask)
+    B, H, nK = col.shape
+    out = np.zeros(nK, dtype=np.int64)
+    for b in range(B):
+        for h in range(H):
+            out += col[b, h]
+    return out

@@ -80,6 +80,26 @@ def test_plan_host_validation(built_library, args, expect):
     assert dbsp.library().dbsp_plan_lpt(*args) == expect
 
 
+@pytest.mark.parametrize("bc,ic,expect", [(0, 0, 1), (-2, 0, 1), (70000, 0, 1), (1, -1, 1), (1, 1 << 25, 1)])
+def test_plan_cost_host_validation(built_library, bc, ic, expect):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_plan_lpt_cost(FAKE, None, 10, 4, 0, bc, ic, FAKE, FAKE, FAKE, None, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, 2, 8, FAKE, None), 1),      # null column loads
+    ((FAKE, 0, 8, FAKE, None), 1),      # no groups
+    ((FAKE, 2, 0, FAKE, None), 1),      # no columns
+    ((FAKE, 2, 8, None, None), 1),      # null output
+    ((FAKE + 2, 2, 8, FAKE, None), 1),  # misaligned input
+])
+def test_kv_block_loads_host_validation(built_library, args, expect):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_kv_block_loads(*args) == expect
+
+
 def _attn_args(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, mask=FAKE, B=1, H=1, S=256, d=128, block=128, causal=0, scale=0.0,
              off=FAKE, wl=FAKE, nw=4, out=FAKE, lse=None, op=None, mp=None, lp=None, tim=None, st=None)

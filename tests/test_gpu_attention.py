@@ -185,6 +185,36 @@ def test_sharded_merge_equals_unsharded(built_library, cuda_device, layout):
     _check_sampled(w, mask_np, q, k, v, out, lse, items)
 
 
+def test_lpt_kv_shards(built_library, cuda_device):
+    """KV blocks planned over shards by LPT of their column loads (db-SP blog, scenario
+    2): the plan is the oracle's LPT, the shards partition the dense blocks, and the
+    merged partials equal the unsharded output."""
+    from oracle import loads as OL
+    from oracle import lpt as OP
+
+    w = W.WORKLOADS["sharded"]
+    mask_np, mask, q, k, v = _gpu_problem(w)
+    n_sh = w.extra["n_shards"]
+    sp = P.plan_kv_shards(mask, n_sh)
+    ref = OP.lpt_plan(OL.kv_block_loads(mask_np), n_sh)
+    np.testing.assert_array_equal(sp.shard_of.cpu().numpy(), ref["worker_of"])
+    np.testing.assert_array_equal(sp.shard_offsets.cpu().numpy(), ref["offsets"])
+    np.testing.assert_array_equal(sp.shard_blocks.cpu().numpy(), ref["worklist"])
+    np.testing.assert_array_equal(sp.shard_loads.cpu().numpy(), ref["worker_loads"])
+    shards = P.shard_masks_from_plan(mask, sp)
+    assert int((shards != 0).sum().item()) == int((mask_np != 0).sum())
+    m = P.default_workers()
+    out_ref, lse_ref = P.attention(q, k, v, mask, w.block, w.causal, P.plan(mask, m))
+    out, lse, _ = P.sharded_attention(q, k, v, shards, w.block, w.causal, m)
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.dbsp_device_status() == 0
+    assert_rows_close(to64(out).reshape(-1, w.d), to64(out_ref).reshape(-1, w.d),
+                      to64(lse).reshape(-1), to64(lse_ref).reshape(-1), what="lpt shards vs unsharded")
+    items = sample_items(mask_np, 12, 2, seed=9)
+    _check_sampled(w, mask_np, q, k, v, out, lse, items)
+
+
 def test_cta_timing_counts_dense_blocks(built_library, cuda_device):
     w, mask_np = _small(128, 128, True, seed=31)
     q, k, v = (t.to(DEV) for t in W.make_qkv(w, "cpu"))

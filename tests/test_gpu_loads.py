@@ -63,3 +63,18 @@ def test_unaligned_mask_pointer_takes_byte_path(built_library, cuda_device):
     r, c, _ = OL.block_mask_loads(mask_np)
     np.testing.assert_array_equal(row.cpu().numpy(), r)
     np.testing.assert_array_equal(col.cpu().numpy(), c)
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_kv_block_loads(built_library, cuda_device, name):
+    from load_balancing_gb300 import dbsp
+
+    mask_np = W.make_mask(W.WORKLOADS[name])
+    B, H, nQ, nK = mask_np.shape
+    row = torch.empty((B, H, nQ), dtype=torch.int32, device="cuda:0")
+    col = torch.empty((B, H, nK), dtype=torch.int32, device="cuda:0")
+    dbsp.dbsp_block_mask_loads(torch.from_numpy(mask_np).cuda(), row, col)
+    kv = torch.full((nK,), -3, dtype=torch.int32, device="cuda:0")
+    dbsp.dbsp_kv_block_loads(col, kv)
+    assert dbsp.dbsp_device_status() == 0
+    np.testing.assert_array_equal(kv.cpu().numpy(), OL.kv_block_loads(mask_np))

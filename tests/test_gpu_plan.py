@@ -127,3 +127,52 @@ def test_key_width_boundary(built_library, cuda_device, m, lo, hi):
         loads = rng.integers(lo, hi, n)
         loads[0] = hi - 1
         _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+
+
+
+@pytest.mark.parametrize("bc,ic", [(1, 0), (1, 1), (8, 1), (16, 3), (1000, 7)])
+def test_cost_model_is_lpt_on_transformed_loads(built_library, cuda_device, bc, ic):
+    """dbsp_plan_lpt_cost plans on loads * block_cost + item_cost: the textbook LPT of
+    the transformed loads (the order of the items is unchanged)."""
+    from load_balancing_gb300 import dbsp
+
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(bc * 31 + ic)
+    for n, m, hi in ((1, 3, 5), (500, 7, 40), (4096, 152, 33), (3000, 300, 3)):
+        loads = rng.integers(0, hi, n)
+        loads[rng.random(n) < 0.3] = 0  # many items without dense blocks
+        lt = torch.as_tensor(loads.astype(np.int32)).to(dev)
+        wo = torch.empty(n, dtype=torch.int32, device=dev)
+        off = torch.empty(m + 1, dtype=torch.int32, device=dev)
+        wl = torch.empty(n, dtype=torch.int32, device=dev)
+        wload = torch.empty(m, dtype=torch.int64, device=dev)
+        dbsp.dbsp_plan_lpt_cost(lt, m, bc, ic, wo, off, wl, wload)
+        assert dbsp.dbsp_device_status() == 0
+        got = {"worker_of": wo.cpu().numpy(), "offsets": off.cpu().numpy(), "worklist": wl.cpu().numpy(),
+               "worker_loads": wload.cpu().numpy()}
+        _assert_same(got, OP.lpt_plan(loads.astype(np.int64) * bc + ic, m))
+
+
+def test_item_cost_spreads_empty_items(built_library, cuda_device):
+    """With block costs only, every item without dense blocks goes to the least-loaded
+    worker; with an item cost the empty items are spread so that the planning loads
+    balance to within one item."""
+    from load_balancing_gb300 import dbsp
+
+    dev = torch.device("cuda:0")
+    loads = np.zeros(1000, dtype=np.int32)
+    loads[:50] = 10
+    m = 20
+    lt = torch.as_tensor(loads).to(dev)
+    counts, wloads = [], []
+    for bc, ic in ((1, 0), (8, 1)):
+        wo = torch.empty(1000, dtype=torch.int32, device=dev)
+        off = torch.empty(m + 1, dtype=torch.int32, device=dev)
+        wl = torch.empty(1000, dtype=torch.int32, device=dev)
+        wload = torch.empty(m, dtype=torch.int64, device=dev)
+        dbsp.dbsp_plan_lpt_cost(lt, m, bc, ic, wo, off, wl, wload)
+        counts.append(np.bincount(wo.cpu().numpy(), minlength=m))
+        wloads.append(wload.cpu().numpy())
+    assert counts[0].max() >= 950  # the zero loads pile onto one worker
+    assert counts[1].max() <= 100  # spread over the workers
+    assert wloads[1].max() - wloads[1].min() <= 10 * 8 + 1  # planning loads within one item

@@ -104,3 +104,17 @@ def test_causal_ring_nonempty_pairs(n_shards):
         assert nonempty == g["nonempty_pairs"]
         assert n_shards * n_shards == g["total_pairs"]
     assert len(shards) == n_shards
+
+
+def test_kv_block_loads_closed_form_and_total():
+    """Full causal mask on every head: column j of each head has nQ - j dense blocks,
+    so the KV-block load over B*H heads is B*H*(nQ - j); the loads sum to the total."""
+    w = W.WORKLOADS["sharded"]
+    mask = W.make_mask(w)[:, :3]
+    kv = L.kv_block_loads(mask)
+    np.testing.assert_array_equal(kv, 3 * (w.nQ - np.arange(w.nK)))
+    rng = np.random.default_rng(5)
+    m2 = (rng.random((2, 3, 9, 11)) < 0.4).astype(np.uint8)
+    kv2 = L.kv_block_loads(m2)
+    assert kv2.sum() == (m2 != 0).sum()
+    np.testing.assert_array_equal(kv2, (m2 != 0).sum(axis=(0, 1, 2)))
