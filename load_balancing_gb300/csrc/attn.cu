@@ -25,16 +25,17 @@
 //               once PV(G-3) has completed;
 //   warp 3      lane 0 issues O += P(G) V_G (M=128 N=d K=block, P from TMEM, V from
 //               shared memory, MN-major) once the softmax has stored P(G);
-//   warps 4..7  softmax of S columns [0, block/2) and O columns [0, d/2); warps 8..11
-//               of the other halves. Thread = query row = TMEM lane. tcgen05.ld of
-//               the half row, diagonal masking, the half-row maxima are exchanged
-//               through shared memory (bounded mbarrier) so both halves share one
-//               running maximum (base-2 units); P = exp2(S*scale*log2e - m) rounded
-//               to bf16 pairs and stored into TMEM with tcgen05.st. O is rescaled in
-//               TMEM only when a row's maximum grows by more than 2^8 (exact either
-//               way: O and l always share one reference maximum), after waiting for
-//               the previous PV. Epilogue: O / l and LSE, or the partial triple with
-//               the true row maximum; an empty partial writes only m = -inf, l = 0.
+//   warps 4..11 softmax: warp 4 + 4 s + q owns the 16 query rows q*32 + s*16 + [0, 16)
+//               (TMEM lanes of quarter q). A row is split over two threads of one warp
+//               (split 16-lane tcgen05 shape): one holds S columns [0, block/2) and O
+//               columns [0, d/2), the other the second halves, so the row maximum and
+//               the row sum take one shuffle and no warp waits on another. Diagonal
+//               masking; running maximum in base-2 units; P = exp2(S*scale*log2e - m)
+//               rounded to bf16 pairs and stored into TMEM with tcgen05.st. O is
+//               rescaled in TMEM only when a row's maximum grows by more than 2^8
+//               (exact either way: O and l always share one reference maximum), after
+//               waiting for the previous PV. Epilogue: O / l and LSE, or the partial
+//               triple with the true row maximum.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer). On expiry the CTA sets the
 // device error word to DBSP_ERR_TIMEOUT, every role leaves its loop, in-flight
@@ -110,15 +111,12 @@ struct alignas(8) Ctrl {
   uint64_t k_full[kKStages];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t item_full[2], item_empty[2];
-  uint64_t xbar[2], lbar[2];      // row-max (per block) and row-sum (per item) exchange
   uint64_t drain;
   int item_id[2], item_n[2], item_diag[2];
   alignas(4) uint16_t scan_bits[2][32];  // producers: dense bits of one 512-column mask chunk
   uint32_t tmem_base;
   volatile int abort_flag;
   long long blocks_done;
-  float xmax[2][2][128];          // [block parity][column half][row]
-  float xsum[2][2][128];          // [item parity][column half][row]
 };
 
 template <int BLOCK, int D>
@@ -459,24 +457,25 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Softmax warpgroups: warps 4..7 own columns [0, BLOCK/2) of every S row and columns
-// [0, D/2) of O; warps 8..11 own the other halves. Both halves of a row see the
-// same row maximum through a shared-memory exchange behind a bounded mbarrier, so
-// their rescale decisions agree; the row sum is combined once per item.
+// Softmax warps: warp 4 + 4 * sub + quarter owns the 16 rows quarter * 32 + sub * 16 + [0, 16)
+// of the tile (TMEM lanes of its quarter). Each row is split over two threads of the same
+// warp (split 16-lane TMEM shape): thread t < 16 holds columns [0, BLOCK/2) of S and
+// [0, D/2) of O for row t, thread t + 16 the other halves. Row maxima and row sums are
+// combined with one shuffle, so the softmax warps never wait on one another.
 template <int BLOCK, int D>
 __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
   constexpr int CW = BLOCK / 2;  // S columns per thread
   constexpr int DW = D / 2;      // O columns per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int half = (warp - kSoftmaxWarp0) >> 2;
-  const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
+  const int sub = (warp - kSoftmaxWarp0) >> 2;
+  const int ch = lane >> 4;                          // column half of this thread
+  const int r = quarter * 32 + sub * 16 + (lane & 15);  // query row within the tile = TMEM lane
   const bool row_ok = r < BLOCK;
-  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-  const uint32_t o_off = half * DW;
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32 + sub * 16) << 16);
   const bool partial = p.o_part != nullptr;
   const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
-  uint32_t items = 0, G = 0, items_done = 0;
+  uint32_t items = 0, G = 0;
   bool ok = true;
   while (ok) {
     const uint32_t slot = items & 1;
@@ -489,35 +488,23 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     const long long bh = item / p.nQ;
     const int qb = item % p.nQ;
     const long long grow = bh * p.S + (long long)qb * BLOCK + r;  // global query row
-    if (n == 0) {
-      if (row_ok) {
-        if (partial) {
-          // (m, l) = (-inf, 0) marks the partial empty; its O rows are never read
-          if (half == 0) { p.m_part[grow] = -INFINITY; p.l_part[grow] = 0.f; }
-        } else {
-          uint4* o = reinterpret_cast<uint4*>(p.out + grow * D + half * DW);
-#pragma unroll
-          for (int i = 0; i < DW / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-          if (half == 0 && p.lse) p.lse[grow] = -INFINITY;
-        }
-      }
-      continue;
-    }
+    if (n == 0) continue;  // empty items are written by the producer and never published
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
     for (int j = 0; j < n; ++j, ++G) {
-      const uint32_t b = G % kSBufs, bu = G / kSBufs, xs = G & 1;
+      const uint32_t b = G % kSBufs, bu = G / kSBufs;
       const uint32_t sbase = lane_base + kSCol + b * 128;
       if (!wait_bar(c, smem_u32(&c->s_full[b]), bu & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[CW];
-      if constexpr (CW == 64) tmem_ld64_wait(sbase + half * CW, sr);
-      else tmem_ld32_wait(sbase + half * CW, sr);
+      if constexpr (CW == 64) tmem_ld64s_wait<CW>(sbase, sr);
+      else tmem_ld32s_wait<CW>(sbase, sr);
       float* s = reinterpret_cast<float*>(sr);
       if (diag && j == n - 1) {
 #pragma unroll
-        for (int k = 0; k < CW; ++k) if (half * CW + k > r) s[k] = -INFINITY;
+        for (int k = 0; k < CW; ++k) if (ch * CW + k > r) s[k] = -INFINITY;
       }
-      // half-row maximum (3-input max, 4 independent chains)
+      // row maximum: 3-input max over this thread's half (4 independent chains), then
+      // one shuffle with the thread holding the other half of the row
       static_assert(CW % 8 == 0, "half rows come in multiples of 8 columns");
       float mxa[4];
 #pragma unroll
@@ -528,13 +515,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
         for (int q = 0; q < 4; ++q) mxa[q] = max3(mxa[q], s[k + 2 * q], s[k + 2 * q + 1]);
       }
       const float mh = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
-      c->xmax[xs][half][r] = mh;
-      tc_fence_before();  // this half's S reads precede the other half's P writes
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->xbar[xs]));
-      if (!wait_bar(c, smem_u32(&c->xbar[xs]), (G >> 1) & 1, p.err)) { ok = false; break; }
-      tc_fence_after();
-      const float mx = fmaxf(mh, c->xmax[xs][half ^ 1][r]);
+      const float mx = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
 
       float alpha = 1.f;
       bool rescale = false;
@@ -567,9 +548,10 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
         f2_unpack(t, t0, t1);
         l += t0 + t1;
       }
-      // P over this half's share of the first BLOCK/2 columns of the S buffer
-      if constexpr (CW == 64) tmem_st32(sbase + half * (CW / 2), pk);
-      else tmem_st16(sbase + half * (CW / 2), pk);
+      // P (bf16 pairs) over the first BLOCK/2 columns of the S buffer; the S columns it
+      // overwrites were read by this same warp above
+      if constexpr (CW == 64) tmem_st32s<CW / 2>(sbase, pk);
+      else tmem_st16s<CW / 2>(sbase, pk);
       if (__any_sync(0xffffffffu, rescale)) {
         // O may be touched only once PV of the previous block is complete
         const uint32_t gp = G - 1, pb = gp % kSBufs;
@@ -577,11 +559,11 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
         tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < DW / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32_wait(lane_base + o_off + cc * 32, o);
+          uint32_t t[32];
+          tmem_ld32s_wait<DW>(lane_base + cc * 32, t);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-          tmem_st32(lane_base + o_off + cc * 32, o);
+          for (int q = 0; q < 32; ++q) t[q] = __float_as_uint(__uint_as_float(t[q]) * alpha);
+          tmem_st32s<DW>(lane_base + cc * 32, t);
         }
       }
       tmem_wait_st();
@@ -590,39 +572,32 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
       if (lane == 0) mbar_arrive(smem_u32(&c->p_full[b]));
     }
     if (!ok) break;
-    // row sum of both halves (once per item)
-    const uint32_t lb = items_done & 1;
-    c->xsum[lb][half][r] = l;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&c->lbar[lb]));
-    if (!wait_bar(c, smem_u32(&c->lbar[lb]), (items_done >> 1) & 1, p.err)) break;
-    l += c->xsum[lb][half ^ 1][r];
-    ++items_done;
+    l += __shfl_xor_sync(0xffffffffu, l, 16);  // row sum over both halves
     // epilogue: wait for the last PV of this item; the next item's first PV waits for
     // these warps' P, which they store only after the reads below
     const uint32_t gl = G - 1;
     if (!wait_bar(c, smem_u32(&c->pv_done[gl % kSBufs]), (gl / kSBufs) & 1, p.err)) break;
     tc_fence_after();
     uint32_t o[DW];
-    if constexpr (DW == 64) tmem_ld64_wait(lane_base + o_off, o);
-    else tmem_ld32_wait(lane_base + o_off, o);
+    if constexpr (DW == 64) tmem_ld64s_wait<DW>(lane_base, o);
+    else tmem_ld32s_wait<DW>(lane_base, o);
     tc_fence_before();
     if (row_ok) {
       const float* of = reinterpret_cast<const float*>(o);
       constexpr float kLn2 = 0.693147180559945309f;
       if (partial) {
         const float f = ex2(m_ref - m_true);
-        float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D + half * DW);
+        float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D + ch * DW);
 #pragma unroll
         for (int i = 0; i < DW / 4; ++i)
           dst[i] = make_float4(of[4 * i] * f, of[4 * i + 1] * f, of[4 * i + 2] * f, of[4 * i + 3] * f);
-        if (half == 0) {
+        if (ch == 0) {
           p.m_part[grow] = m_true * kLn2;
           p.l_part[grow] = l * f;
         }
       } else {
         const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * D + half * DW);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * D + ch * DW);
 #pragma unroll
         for (int i = 0; i < DW / 8; ++i) {
           uint4 v;
@@ -632,7 +607,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
           v.w = pack_bf16(of[8 * i + 6] * inv, of[8 * i + 7] * inv);
           dst[i] = v;
         }
-        if (half == 0 && p.lse) p.lse[grow] = (m_ref + __log2f(l)) * kLn2;
+        if (ch == 0 && p.lse) p.lse[grow] = (m_ref + __log2f(l)) * kLn2;
       }
     }
   }
@@ -664,8 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&c->item_full[i]), 1);
       mbar_init(smem_u32(&c->item_empty[i]), 9);  // MMA issuer + 8 softmax warps
-      mbar_init(smem_u32(&c->xbar[i]), 8);
-      mbar_init(smem_u32(&c->lbar[i]), 8);
     }
     mbar_init(smem_u32(&c->drain), 2);  // one commit per MMA issuer
     c->abort_flag = 0;
