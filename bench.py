@@ -568,6 +568,55 @@ def run_suite(args):
     return 0
 
 
+def run_kernels_once(args):
+    """One launch each of the mask-loads, LPT-plan and merge kernels (a profiler target).
+
+    Mask loads on the imbalance workload's mask (41.9 MB), the plan over the LLM-heads
+    workload's 2,048 row loads, and the merge of 8 fp32 partials of 131,072 rows x 128
+    (20 % of them empty, m = -inf, l = 0).
+    """
+    import torch
+
+    from load_balancing_gb300 import dbsp
+    from load_balancing_gb300 import path as P
+    from load_balancing_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wi = W.WORKLOADS["imbalance"]
+    mask = torch.from_numpy(W.make_mask(wi)).to(dev)
+    row = torch.empty((wi.B, wi.H, wi.nQ), dtype=torch.int32, device=dev)
+    col = torch.empty((wi.B, wi.H, wi.nK), dtype=torch.int32, device=dev)
+    head = torch.empty((wi.B, wi.H), dtype=torch.int32, device=dev)
+    wl = W.WORKLOADS["llm"]
+    lrow = torch.from_numpy(W.make_mask(wl)).to(dev).ne(0).sum(-1, dtype=torch.int32).reshape(-1).contiguous()
+    m = P.default_workers(dev)
+    n = lrow.numel()
+    wo = torch.empty(n, dtype=torch.int32, device=dev)
+    off = torch.empty(m + 1, dtype=torch.int32, device=dev)
+    wlst = torch.empty(n, dtype=torch.int32, device=dev)
+    wload = torch.empty(m, dtype=torch.int64, device=dev)
+    rows, d, ns = 131072, 128, 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    o = torch.randn((ns, rows, d), generator=g, device=dev)
+    mm = torch.randn((ns, rows), generator=g, device=dev) * 4
+    ll = torch.rand((ns, rows), generator=g, device=dev) * 50 + 0.5
+    empty = torch.rand((ns, rows), generator=g, device=dev) < 0.2
+    mm[empty] = -float("inf")
+    ll[empty] = 0
+    out = torch.empty((rows, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    dbsp.dbsp_block_mask_loads(mask, row, col, head)
+    dbsp.dbsp_plan_lpt(lrow, m, wo, off, wlst, wload)
+    dbsp.dbsp_merge_partials(o, mm, ll, out, lse)
+    torch.cuda.synchronize()
+    status = dbsp.dbsp_device_status()
+    print(json.dumps({"profile_kernels": ["mask_loads", "lpt_plan", "merge_partials"], "device_status": status}))
+    return 0 if status == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -577,6 +626,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true", help="one line per workload, every kernel timed alone")
     ap.add_argument("--workloads", default="", help="comma-separated workload names for --suite")
+    ap.add_argument("--profile-kernels", action="store_true",
+                    help="launch the mask-loads, plan and merge kernels once each (for a profiler)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
@@ -584,6 +635,8 @@ def main():
         return run_reference(args)
     if args.suite:
         return run_suite(args)
+    if args.profile_kernels:
+        return run_kernels_once(args)
     return run_gpu(args)
 
 

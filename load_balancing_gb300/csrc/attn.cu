@@ -69,8 +69,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                // S buffers at TMEM columns 128, 256, 384
 constexpr uint32_t kSCol = 128;
 constexpr int kQBufs = 2;
-constexpr int kKStages = 2;
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
+// a ring stage is reused after the S (K) or PV (V) that read it completed, tested on the
+// per-S-buffer barriers: a ring may not be deeper than the S buffers
+static_assert(kKStages <= kSBufs && kVStages <= kSBufs, "ring deeper than the S buffers");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;    // 100 ms per teardown wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: P <= 256 between rescales
@@ -471,7 +474,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
   const int sub = (warp - kSoftmaxWarp0) >> 2;
   const int ch = lane >> 4;                          // column half of this thread
   const int r = quarter * 32 + sub * 16 + (lane & 15);  // query row within the tile = TMEM lane
-  const bool row_ok = r < BLOCK;
+  const bool row_ok = BLOCK == 128 || r < BLOCK;  // a 64-row tile leaves TMEM lanes 64..127 unused
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32 + sub * 16) << 16);
   const bool partial = p.o_part != nullptr;
   const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
@@ -719,6 +722,7 @@ int launch_attn(const void* q, const void* k, const void* v, const AttnParams& p
       encode_map(&tv, v, rows, D, BLOCK))
     return dbsp::cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   constexpr size_t smem = smem_bytes<BLOCK, D>();
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
   auto kernel = attn_fwd_kernel<BLOCK, D>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(attn)");
