@@ -130,6 +130,20 @@ def test_key_width_boundary(built_library, cuda_device, m, lo, hi):
 
 
 
+@pytest.mark.parametrize("m", [1, 2, 3, 33, 152, 1024])
+def test_bucket_ring_edges(built_library, cuda_device, m):
+    """Loads far apart (one huge item among tiny ones, long runs of equal loads) make
+    the least-loaded worker win many picks in a row and move workers across the whole
+    load ring; the plan stays the textbook LPT."""
+    rng = np.random.default_rng(m + 77)
+    for n in (2, 9, 300, 3000):
+        loads = rng.choice(np.array([0, 1, 2, 1000]), n, p=[0.2, 0.4, 0.3, 0.1])
+        _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+        loads = rng.integers(0, 64, n)
+        loads[: max(1, n // 50)] = 2047
+        _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+
+
 @pytest.mark.parametrize("bc,ic", [(1, 0), (1, 1), (8, 1), (16, 3), (1000, 7)])
 def test_cost_model_is_lpt_on_transformed_loads(built_library, cuda_device, bc, ic):
     """dbsp_plan_lpt_cost plans on loads * block_cost + item_cost: the textbook LPT of
