@@ -468,7 +468,7 @@ def run_suite(args):
     peaks, peak_src = load_peaks()
     reps = max(3, args.steps)
     names = args.workloads.split(",") if args.workloads else W.ORDER
-    for name in names:
+    for name in [x for x in names if x in W.WORKLOADS]:
         w = W.WORKLOADS[name]
         mask_np = W.make_mask(w)
         n_dense = dense_blocks(mask_np, w.causal)
@@ -565,7 +565,62 @@ def run_suite(args):
         print(json.dumps(line), flush=True)
         del q, k, v, out, lse, mask
         torch.cuda.empty_cache()
+    if not args.workloads or "long_causal" in names:
+        split_study(dev, stream, flush, reps, peaks)
     return 0
+
+
+def split_study(dev, stream, flush, reps, peaks):
+    """Heavy items split along their KV blocks (db-SP blog, closing remark) on rows as
+    heavy as the mean load per SM: two fully causal heads of 16,384 tokens. Whole-item
+    LPT against split LPT (automatic piece load), plan + attention (+ merge) timed."""
+    import torch
+
+    from load_balancing_gb300 import dbsp
+    from load_balancing_gb300 import path as P
+    from load_balancing_gb300 import workloads as W
+
+    w = W.custom("long_causal", 1, 2, 16384, 128, 128, True, 6, 106, "causal_full")
+    mask_np = W.make_mask(w)
+    n_dense = dense_blocks(mask_np, w.causal)
+    flop = 4.0 * w.block * w.block * w.d * n_dense
+    mask = torch.from_numpy(mask_np).to(dev)
+    q, k, v = W.make_qkv(w, dev)
+    m = P.default_workers(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    timing = torch.zeros(3 * m, dtype=torch.int64, device=dev)
+    line = {"suite": True, "workload": f"long_causal: B=1 H=2 S=16384 d=128 block=128 causal=1; full causal mask; "
+                                      f"Q/K/V bf16 N(0,1)", "dense_blocks": n_dense, "items": w.n_items,
+            "n_workers": m, "largest_item": int((mask_np != 0).sum(-1).max()), "mean_per_worker": n_dense / m}
+    pb = P.plan(mask, m, stream=stream)
+    sp = P.plan_split(mask, m, w.block, w.d, stream=stream)
+
+    def skew():
+        tt = timing.view(m, 3).cpu().numpy()
+        busy = (tt[:, 1] - tt[:, 0]).astype(np.float64)
+        return float((busy.max() - busy.mean()) / busy.mean())
+
+    attn = lambda: dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, pb.worker_offsets,
+                                                   pb.worklist, m, out=out, lse=lse, cta_timing=timing,
+                                                   stream=stream)
+    t = _time_ms(attn, stream, flush, reps)
+    line["whole_lpt"] = {"attn_us": 1e3 * t, "TFLOP/s": flop / t / 1e9, "sm_skew": skew(),
+                         "plan_us": 1e3 * _time_ms(lambda: P.plan(mask, m, out=pb, stream=stream), stream, flush,
+                                                   reps)}
+    attn_s = lambda: P.attention_split(q, k, v, mask, w.block, w.causal, sp, out=out, lse=lse, cta_timing=timing,
+                                       stream=stream)
+    t_s = _time_ms(attn_s, stream, flush, reps)
+    sk = skew()
+    counts = sp.counts.cpu().numpy().tolist()
+    line["split_lpt"] = {"attn_plus_merge_us": 1e3 * t_s, "TFLOP/s": flop / t_s / 1e9, "sm_skew": sk,
+                         "plan_us": 1e3 * _time_ms(lambda: P.plan_split(mask, m, w.block, w.d, out=sp,
+                                                                        stream=stream), stream, flush, reps),
+                         "units": counts[0], "split_items": counts[2], "pieces": counts[3], "piece_load": counts[4]}
+    line["frac_of_bf16_peak"] = {"whole": flop / t / 1e9 / float(peaks["bf16_tflops"]),
+                                 "split": flop / t_s / 1e9 / float(peaks["bf16_tflops"])}
+    line["device_status"] = dbsp.dbsp_device_status()
+    print(json.dumps(line), flush=True)
 
 
 def run_kernels_once(args):

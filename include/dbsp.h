@@ -138,6 +138,55 @@ DBSP_API int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int n
                        int64_t* worker_loads, void* stream);
 
 /*
+ * LPT plan (as dbsp_plan_lpt_cost, no bonus) over the first *n_items_dev items, the
+ * count living in device memory (e.g. counts[0] of dbsp_split_plan), so that a
+ * plan over a unit table needs no host synchronisation.
+ *
+ *   n_items_dev   int32 [1] device pointer: the item count, clamped to [0, n_items_max].
+ *   n_items_max   >= 0: the capacity of loads, worker_of and worklist.
+ * Every other argument as in dbsp_plan_lpt_cost; worklist and worker_offsets cover
+ * the first *n_items_dev items only.
+ */
+DBSP_API int dbsp_plan_lpt_cost_n(const int32_t* loads, const int32_t* n_items_dev, int n_items_max,
+                         int n_workers, int32_t block_cost, int32_t item_cost, int32_t* worker_of,
+                         int32_t* worker_offsets, int32_t* worklist, int64_t* worker_loads,
+                         void* stream);
+
+/*
+ * Split plan: heavy items cut into pieces along their KV blocks.  [db-SP blog,
+ * scenario 1]: the greedy cannot balance perfectly, partly because an item's load
+ * cannot be divided; the page's closing remark points at splitting the load
+ * further. Item i with load L = loads[i] > T becomes k = min(ceil(L / T), max_pieces)
+ * pieces; piece j takes the row's dense blocks whose rank (column order, within the
+ * causal limit) lies in [floor(j L / k), floor((j + 1) L / k)). Every other item
+ * stays whole (k = 1).
+ *
+ *   loads          int32 [n_items] >= 0 (dense blocks per item within its causal
+ *                  limit, e.g. row loads of dbsp_block_mask_loads for a causal mask
+ *                  without blocks above the diagonal).
+ *   n_workers      >= 1: used by the automatic T.
+ *   max_piece_load T; <= 0 selects T = ceil(ceil(total / n_workers) / 2).
+ *   max_pieces     in [1, 1024];  max_slots >= 0: capacity for pieces.
+ * Outputs (device, written by one single-CTA kernel):
+ *   unit_item, unit_pk, unit_slot, unit_load  int32 [n_items * max_pieces]: the
+ *                  unit table. Units [0, n_whole) are the whole items in item order
+ *                  (pk = 1 << 16, slot = -1); unit n_whole + s is piece slot s, the
+ *                  pieces of each split item consecutive in j (pk = j | k << 16).
+ *                  unit_load: the unit's dense blocks.
+ *   split_item     int32 [n_items]: the split items in item order.
+ *   split_off      int32 [n_items + 1]: slots of split item t are
+ *                  split_off[t] .. split_off[t + 1] - 1.
+ *   counts         int32 [5]: units U = n_whole + n_slots, n_whole, n_split,
+ *                  n_slots, T.
+ * A negative load sets DBSP_ERR_INVALID_ARG, more than max_slots pieces
+ * DBSP_ERR_UNSUPPORTED, on the device; counts are then zero.
+ */
+DBSP_API int dbsp_split_plan(const int32_t* loads, int n_items, int n_workers, int32_t max_piece_load,
+                    int32_t max_pieces, int32_t max_slots, int32_t* unit_item, int32_t* unit_pk,
+                    int32_t* unit_slot, int32_t* unit_load, int32_t* split_item, int32_t* split_off,
+                    int32_t* counts, void* stream);
+
+/*
  * Block-sparse attention forward over an LPT worklist.  [6D notes §2.1, step 2]:
  * a chunk of keys yields the unnormalised output O, the row maximum m and the
  * row sum l of the softmax numerators; the result is O / l (last line of the
@@ -177,6 +226,47 @@ DBSP_API int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const void
                                void* out, float* lse,
                                float* o_part, float* m_part, float* l_part,
                                int64_t* cta_timing, void* stream);
+
+/*
+ * Block-sparse attention forward over a worklist of units (dbsp_split_plan).  Each
+ * worklist entry u < n_units names piece j of k of item unit_item[u]
+ * (unit_pk[u] = j | k << 16). A whole item (k = 1) is written to out / lse as in
+ * dbsp_block_sparse_attn_fwd's final mode; a piece attends only to its dense blocks
+ * (ranks [floor(j L / k), floor((j + 1) L / k)) of the row's L) and writes its
+ * unnormalised partial, as in partial mode, to slot s = unit_slot[u]:
+ *   o_piece  fp32 [max_slots, block, d]; m_piece, l_piece fp32 [max_slots, block]; a
+ *            piece without dense blocks writes only (m, l) = (-inf, 0). A slot
+ *            outside [0, max_slots) sets DBSP_ERR_INVALID_ARG and the unit is skipped.
+ * The causal diagonal block, the last dense block of its row, is masked by the piece
+ * that holds it (j = k - 1). Combine the pieces with dbsp_merge_pieces.
+ * Every other argument as in dbsp_block_sparse_attn_fwd (final mode only). An entry
+ * outside [0, n_units) or an inconsistent unit sets DBSP_ERR_INVALID_ARG on the
+ * device.
+ */
+DBSP_API int dbsp_block_sparse_attn_fwd_units(const void* q, const void* k, const void* v,
+                                     const uint8_t* mask, int B, int H, int S, int d, int block,
+                                     int causal, float scale,
+                                     const int32_t* worker_offsets, const int32_t* worklist,
+                                     int n_workers, const int32_t* unit_item,
+                                     const int32_t* unit_pk, const int32_t* unit_slot, int n_units,
+                                     void* out, float* lse, float* o_piece, float* m_piece,
+                                     float* l_piece, int max_slots, int64_t* cta_timing, void* stream);
+
+/*
+ * Merge of the pieces of split items.  [6D notes §2.1, step 3 and the final
+ * division], as dbsp_merge_partials, over the slots of each split item: for split
+ * item t (t < counts[2]) and row r of its Q-block, the partials at rows
+ * s * block + r of o_piece / m_piece / l_piece, s in [split_off[t], split_off[t + 1]),
+ * give out[item row r] (bf16) and lse (natural log; -inf and O = 0 when every piece
+ * is empty). Rows of whole items are not touched.
+ *
+ *   split_item, split_off, counts: as written by dbsp_split_plan (device).
+ *   out bf16 [B, H, S, d], lse fp32 [B, H, S] or NULL; d in {64, 128}.
+ * A split entry out of range sets DBSP_ERR_INVALID_ARG on the device.
+ */
+DBSP_API int dbsp_merge_pieces(const float* o_piece, const float* m_piece, const float* l_piece,
+                      const int32_t* split_item, const int32_t* split_off, const int32_t* counts,
+                      int B, int H, int S, int d, int block, void* out, float* lse, void* stream);
 
 /*
  * Merge of KV-shard partials.  [6D notes §2.1, step 3 and the final division]:

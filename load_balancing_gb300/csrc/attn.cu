@@ -92,6 +92,17 @@ struct AttnParams {
   float* l_part;
   int64_t* timing;
   int* err;
+  // units (optional): worklist entries index a unit table; unit u is piece
+  // j = unit_pk[u] & 0xffff of k = unit_pk[u] >> 16 of item unit_item[u], written as a
+  // partial to slot unit_slot[u] (k > 1) or as the item's output (k = 1)
+  const int32_t* unit_item;
+  const int32_t* unit_pk;
+  const int32_t* unit_slot;
+  int n_units;
+  int max_slots;  // capacity of the piece buffers, in slots
+  float* o_piece;
+  float* m_piece;
+  float* l_piece;
 };
 
 template <int BLOCK, int D>
@@ -115,7 +126,7 @@ struct alignas(8) Ctrl {
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
-  int item_id[2], item_n[2], item_diag[2];
+  int item_id[2], item_n[2], item_diag[2], item_slot[2];
   alignas(4) uint16_t scan_bits[2][32];  // producers: dense bits of one 512-column mask chunk
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -238,28 +249,56 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
   const CUtensorMap* map = which == 0 ? tk : tv;
   bool ok = true;
   for (int idx = begin; idx <= end && ok; ++idx) {
-    int item = -1;
+    int item = -1, pj = 0, pk = 1, pslot = -1;
     if (idx < end) {
-      item = __ldg(p.worklist + idx);
-      if (item < 0 || item >= p.n_items) {
+      const int u = __ldg(p.worklist + idx);
+      bool valid;
+      if (p.unit_item) {
+        valid = u >= 0 && u < p.n_units;
+        if (valid) {
+          item = __ldg(p.unit_item + u);
+          const int pkw = __ldg(p.unit_pk + u);
+          pj = pkw & 0xffff;
+          pk = pkw >> 16;
+          pslot = __ldg(p.unit_slot + u);
+          valid = item >= 0 && item < p.n_items && pk >= 1 && pj < pk &&
+                  (pk == 1 ? pslot < 0 : (pslot >= 0 && pslot < p.max_slots));
+        }
+      } else {
+        item = u;
+        valid = item >= 0 && item < p.n_items;
+      }
+      if (!valid) {
         if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
         continue;
       }
     }
-    int n = 0, limit = 0;
+    // dense blocks of the row within the causal limit: L in all; this unit takes the
+    // dense ranks [lo, hi) (piece j of k: floor(j L / k) .. floor((j + 1) L / k))
+    int n = 0, limit = 0, lo = 0, hi = INT_MAX;
     long long kv_row0 = 0;
     if (item >= 0) {
       kv_row0 = (long long)(item / p.nQ) * p.S;
       limit = rs.limit(item);
-      if (which == 0)
-        for (int c0 = 0; c0 < limit; c0 += 512) n += __reduce_add_sync(kAll, __popc(rs.bits(item, c0, limit)));
+      if (which == 0 || pk > 1) {
+        int L = 0;
+        for (int c0 = 0; c0 < limit; c0 += 512) L += __reduce_add_sync(kAll, __popc(rs.bits(item, c0, limit)));
+        lo = (int)(((long long)pj * L) / pk);
+        hi = (int)(((long long)(pj + 1) * L) / pk);
+        n = hi - lo;
+      }
     }
     if (which == 0 && item >= 0 && n == 0) {
-      // An item without dense blocks never reaches the MMA issuers or the softmax: this
-      // warp writes its rows itself (partial mode: m = -inf, l = 0, O rows untouched;
-      // final mode: O = 0, LSE = -inf).
+      // A unit without dense blocks never reaches the MMA issuers or the softmax: this
+      // warp writes its rows itself (a piece or partial mode: m = -inf, l = 0, O rows
+      // untouched; final mode: O = 0, LSE = -inf).
       const long long row0 = (long long)(item / p.nQ) * p.S + (long long)(item % p.nQ) * BLOCK;
-      if (p.o_part) {
+      if (pslot >= 0) {
+        for (int r = lane; r < BLOCK; r += 32) {
+          p.m_piece[(long long)pslot * BLOCK + r] = -INFINITY;
+          p.l_piece[(long long)pslot * BLOCK + r] = 0.f;
+        }
+      } else if (p.o_part) {
         for (int r = lane; r < BLOCK; r += 32) {
           p.m_part[row0 + r] = -INFINITY;
           p.l_part[row0 + r] = 0.f;
@@ -273,7 +312,9 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
       continue;
     }
     if (which == 0) {  // publish the item
-      const int diag = item >= 0 && p.causal && p.mask[(long long)item * p.nK + item % p.nQ] != 0;
+      // the causal diagonal block is the row's last dense block: only the unit ending
+      // there masks it
+      const int diag = item >= 0 && p.causal && pj == pk - 1 && p.mask[(long long)item * p.nK + item % p.nQ] != 0;
       const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
       if (lane == 0) {
         ok = wait_bar(c, smem_u32(&c->item_empty[slot]), (su & 1) ^ 1, p.err);
@@ -281,6 +322,7 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
           c->item_id[slot] = item;
           c->item_n[slot] = n;
           c->item_diag[slot] = diag;
+          c->item_slot[slot] = pslot;
           mbar_arrive(smem_u32(&c->item_full[slot]));
         }
       }
@@ -306,17 +348,25 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
     } else if (item < 0) {
       break;
     }
-    // the dense K (or V) tiles of the row, in block order
-    for (int c0 = 0; c0 < limit && ok; c0 += 512) {
+    // the dense K (or V) tiles of the unit, in block order
+    int rank = 0;  // dense rank of the next block of the row (lane 0)
+    bool past = false;
+    for (int c0 = 0; c0 < limit && ok && !past; c0 += 512) {
       c->scan_bits[which][lane] = (uint16_t)rs.bits(item, c0, limit);
       __syncwarp();
       if (lane == 0) {
         const uint32_t* words = reinterpret_cast<const uint32_t*>(c->scan_bits[which]);
-        for (int w = 0; w < 16 && ok; ++w) {
+        for (int w = 0; w < 16 && ok && !past; ++w) {
           uint32_t wb = words[w];  // columns c0 + 32 w + [0, 32)
           while (wb && ok) {
             const int col = c0 + 32 * w + (__ffs(wb) - 1);
             wb &= wb - 1;
+            const int rk = rank++;
+            if (rk < lo) continue;
+            if (rk >= hi) {
+              past = true;
+              break;
+            }
             const uint32_t s = t_cnt % kstages;
             if (t_cnt >= kstages) {
               const uint32_t prev = t_cnt - kstages;
@@ -335,6 +385,7 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
         }
       }
       ok = __shfl_sync(kAll, ok, 0);
+      past = __shfl_sync(kAll, past, 0);
       __syncwarp();
     }
   }
@@ -484,6 +535,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     const uint32_t slot = items & 1;
     if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
     const int item = c->item_id[slot], n = c->item_n[slot], diag = c->item_diag[slot];
+    const int pslot = c->item_slot[slot];
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&c->item_empty[slot]));
     ++items;
@@ -588,15 +640,17 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     if (row_ok) {
       const float* of = reinterpret_cast<const float*>(o);
       constexpr float kLn2 = 0.693147180559945309f;
-      if (partial) {
+      if (partial || pslot >= 0) {  // unnormalised partial of a KV shard or of a piece
+        const bool piece = pslot >= 0;
+        const long long prow = piece ? (long long)pslot * BLOCK + r : grow;
         const float f = ex2(m_ref - m_true);
-        float4* dst = reinterpret_cast<float4*>(p.o_part + grow * D + ch * DW);
+        float4* dst = reinterpret_cast<float4*>((piece ? p.o_piece : p.o_part) + prow * D + ch * DW);
 #pragma unroll
         for (int i = 0; i < DW / 4; ++i)
           dst[i] = make_float4(of[4 * i] * f, of[4 * i + 1] * f, of[4 * i + 2] * f, of[4 * i + 3] * f);
         if (ch == 0) {
-          p.m_part[grow] = m_true * kLn2;
-          p.l_part[grow] = l * f;
+          (piece ? p.m_piece : p.m_part)[prow] = m_true * kLn2;
+          (piece ? p.l_piece : p.l_part)[prow] = l * f;
         }
       } else {
         const float inv = 1.f / l;
@@ -733,13 +787,23 @@ int launch_attn(const void* q, const void* k, const void* v, const AttnParams& p
 
 }  // namespace
 
-extern "C" int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const void* v,
-                                          const uint8_t* mask, int B, int H, int S, int d,
-                                          int block, int causal, float scale,
-                                          const int32_t* worker_offsets, const int32_t* worklist,
-                                          int n_workers, void* out, float* lse, float* o_part,
-                                          float* m_part, float* l_part, int64_t* cta_timing,
-                                          void* stream) {
+namespace {
+
+struct Units {
+  const int32_t* item;
+  const int32_t* pk;
+  const int32_t* slot;
+  int n;
+  int max_slots;
+  float* o_piece;
+  float* m_piece;
+  float* l_piece;
+};
+
+int attn_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, int B, int H, int S, int d,
+             int block, int causal, float scale, const int32_t* worker_offsets, const int32_t* worklist,
+             int n_workers, void* out, float* lse, float* o_part, float* m_part, float* l_part,
+             int64_t* cta_timing, const Units& u, void* stream) {
   if (!q || !k || !v || !mask || !worker_offsets || !worklist) return DBSP_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1 || n_workers < 1 || n_workers > (1 << 20)) return DBSP_ERR_INVALID_ARG;
   const bool final_mode = out != nullptr;
@@ -754,7 +818,9 @@ extern "C" int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const vo
   if (!dbsp::aligned(q, 16) || !dbsp::aligned(k, 16) || !dbsp::aligned(v, 16) ||
       (out && !dbsp::aligned(out, 16)) || (o_part && !dbsp::aligned(o_part, 16)) ||
       (lse && !dbsp::aligned(lse, 4)) || (m_part && !dbsp::aligned(m_part, 4)) ||
-      (l_part && !dbsp::aligned(l_part, 4)) || (cta_timing && !dbsp::aligned(cta_timing, 8)))
+      (l_part && !dbsp::aligned(l_part, 4)) || (cta_timing && !dbsp::aligned(cta_timing, 8)) ||
+      (u.o_piece && !dbsp::aligned(u.o_piece, 16)) || (u.m_piece && !dbsp::aligned(u.m_piece, 4)) ||
+      (u.l_piece && !dbsp::aligned(u.l_piece, 4)))
     return DBSP_ERR_INVALID_ARG;
   int dev = 0;
   int st = dbsp::check_device(&dev);
@@ -779,9 +845,47 @@ extern "C" int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const vo
   p.l_part = l_part;
   p.timing = cta_timing;
   p.err = dbsp::error_word(dev);
+  p.unit_item = u.item;
+  p.unit_pk = u.pk;
+  p.unit_slot = u.slot;
+  p.n_units = u.n;
+  p.max_slots = u.max_slots;
+  p.o_piece = u.o_piece;
+  p.m_piece = u.m_piece;
+  p.l_piece = u.l_piece;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (block == 128 && d == 128) return launch_attn<128, 128>(q, k, v, p, rows, n_workers, s);
   if (block == 128 && d == 64) return launch_attn<128, 64>(q, k, v, p, rows, n_workers, s);
   if (block == 64 && d == 128) return launch_attn<64, 128>(q, k, v, p, rows, n_workers, s);
   return launch_attn<64, 64>(q, k, v, p, rows, n_workers, s);
+}
+
+}  // namespace
+
+extern "C" int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const void* v,
+                                          const uint8_t* mask, int B, int H, int S, int d,
+                                          int block, int causal, float scale,
+                                          const int32_t* worker_offsets, const int32_t* worklist,
+                                          int n_workers, void* out, float* lse, float* o_part,
+                                          float* m_part, float* l_part, int64_t* cta_timing,
+                                          void* stream) {
+  const Units none{nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr};
+  return attn_fwd(q, k, v, mask, B, H, S, d, block, causal, scale, worker_offsets, worklist, n_workers, out,
+                  lse, o_part, m_part, l_part, cta_timing, none, stream);
+}
+
+extern "C" int dbsp_block_sparse_attn_fwd_units(const void* q, const void* k, const void* v,
+                                                const uint8_t* mask, int B, int H, int S, int d,
+                                                int block, int causal, float scale,
+                                                const int32_t* worker_offsets, const int32_t* worklist,
+                                                int n_workers, const int32_t* unit_item,
+                                                const int32_t* unit_pk, const int32_t* unit_slot,
+                                                int n_units, void* out, float* lse, float* o_piece,
+                                                float* m_piece, float* l_piece, int max_slots,
+                                                int64_t* cta_timing, void* stream) {
+  if (!unit_item || !unit_pk || !unit_slot || n_units < 0 || max_slots < 0 || !out) return DBSP_ERR_INVALID_ARG;
+  if (!o_piece || !m_piece || !l_piece) return DBSP_ERR_INVALID_ARG;
+  const Units u{unit_item, unit_pk, unit_slot, n_units, max_slots, o_piece, m_piece, l_piece};
+  return attn_fwd(q, k, v, mask, B, H, S, d, block, causal, scale, worker_offsets, worklist, n_workers, out,
+                  lse, nullptr, nullptr, nullptr, cta_timing, u, stream);
 }

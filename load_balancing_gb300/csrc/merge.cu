@@ -100,6 +100,70 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
   }
 }
 
+// The pieces of every split item (slots split_off[s] .. split_off[s + 1] - 1, each
+// `block` rows of o/m/l) combined into the item's output rows, with the same one-shot
+// form as above. One warp per output row, four consecutive columns per lane (d <= 128);
+// the number of split items is read from counts[2] on the device, so the grid strides
+// over an upper bound.
+__global__ void __launch_bounds__(kThreads) merge_pieces_kernel(
+    const float* __restrict__ o_piece, const float* __restrict__ m_piece, const float* __restrict__ l_piece,
+    const int32_t* __restrict__ split_item, const int32_t* __restrict__ split_off,
+    const int32_t* __restrict__ counts, int n_items, int nQ, int S, int block, int d,
+    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int n_split = counts[2];
+  if (n_split < 0 || n_split > n_items) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) dbsp::report(err, DBSP_ERR_INVALID_ARG);
+    return;
+  }
+  const long long rows = (long long)n_split * block;
+  const long long warps = (long long)gridDim.x * (kThreads / 32);
+  for (long long row = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); row < rows; row += warps) {
+    const int si = (int)(row / block), r = (int)(row - (long long)si * block);
+    const int item = split_item[si], s0 = split_off[si], s1 = split_off[si + 1];
+    if (item < 0 || item >= n_items || s0 < 0 || s1 < s0) {
+      if (lane == 0) dbsp::report(err, DBSP_ERR_INVALID_ARG);
+      continue;
+    }
+    const long long grow = (long long)(item / nQ) * S + (long long)(item % nQ) * block + r;
+    float mstar = -INFINITY;
+    for (int sl = s0; sl < s1; ++sl) {
+      const long long pr = (long long)sl * block + r;
+      const float mk = __ldg(m_piece + pr), lk = __ldg(l_piece + pr);
+      if (lk > 0.f && mk > -INFINITY) mstar = fmaxf(mstar, mk);
+    }
+    const int c = lane * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
+    if (mstar > -INFINITY) {
+      for (int sl = s0; sl < s1; ++sl) {
+        const long long pr = (long long)sl * block + r;
+        const float mk = __ldg(m_piece + pr), lk = __ldg(l_piece + pr);
+        if (!(lk > 0.f && mk > -INFINITY)) continue;  // an empty piece's O is never read
+        const float w = expf(mk - mstar);
+        l += w * lk;
+        if (c < d) {
+          const float4 x = __ldcs(reinterpret_cast<const float4*>(o_piece + pr * d + c));
+          acc.x += w * x.x;
+          acc.y += w * x.y;
+          acc.z += w * x.z;
+          acc.w += w * x.w;
+        }
+      }
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (c < d) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&a);
+      v.y = *reinterpret_cast<const uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(out + grow * d + c) = v;
+    }
+    if (lse && lane == 0) lse[grow] = l > 0.f ? mstar + logf(l) : -INFINITY;
+  }
+}
+
 }  // namespace
 
 extern "C" int dbsp_merge_partials(const float* o_parts, const float* m_parts, const float* l_parts,
@@ -121,5 +185,27 @@ extern "C" int dbsp_merge_partials(const float* o_parts, const float* m_parts, c
   merge_partials_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       o_parts, m_parts, l_parts, n_shards, rows, d, static_cast<__nv_bfloat16*>(out), lse);
   DBSP_LAUNCH_CHECK("launch merge_partials");
+  return DBSP_OK;
+}
+
+extern "C" int dbsp_merge_pieces(const float* o_piece, const float* m_piece, const float* l_piece,
+                                 const int32_t* split_item, const int32_t* split_off, const int32_t* counts,
+                                 int B, int H, int S, int d, int block, void* out, float* lse, void* stream) {
+  if (B < 1 || H < 1 || S < 1 || (d != 64 && d != 128) || block < 1 || S % block != 0) return DBSP_ERR_INVALID_ARG;
+  if (!o_piece || !m_piece || !l_piece || !split_item || !split_off || !counts || !out) return DBSP_ERR_INVALID_ARG;
+  if (!dbsp::aligned(o_piece, 16) || !dbsp::aligned(out, 8) || !dbsp::aligned(m_piece, 4) ||
+      !dbsp::aligned(l_piece, 4) || (lse && !dbsp::aligned(lse, 4)))
+    return DBSP_ERR_INVALID_ARG;
+  const long long n_items = (long long)B * H * (S / block);
+  if ((long long)B * H * S >= (1LL << 31)) return DBSP_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = dbsp::check_device(&dev);
+  if (st != DBSP_OK) return st;
+  const long long want = (n_items * block + (kThreads / 32) - 1) / (kThreads / 32);
+  const int blocks = (int)std::max<long long>(1, std::min<long long>(want, (long long)dbsp::sm_count(dev) * 8));
+  merge_pieces_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      o_piece, m_piece, l_piece, split_item, split_off, counts, (int)n_items, S / block, S, block, d,
+      static_cast<__nv_bfloat16*>(out), lse, dbsp::error_word(dev));
+  DBSP_LAUNCH_CHECK("launch merge_pieces");
   return DBSP_OK;
 }

@@ -300,9 +300,11 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
 
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
-    const int32_t* __restrict__ loads, const int32_t* __restrict__ home, int n, int m,
+    const int32_t* __restrict__ loads, const int32_t* __restrict__ home, int n_max, const int32_t* n_dev, int m,
     int bonus, int bc, int ic, int32_t* __restrict__ worker_of, int32_t* __restrict__ offsets,
     int32_t* __restrict__ worklist, int64_t* __restrict__ worker_loads, int* err) {
+  // the item count: n_max, or the first *n_dev items when the count lives on the device
+  const int n = n_dev ? min(n_max, max(0, *n_dev)) : n_max;
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ PlanShared sh;
   __shared__ int counts[DBSP_MAX_WORKERS + 1];
@@ -461,12 +463,13 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
 }
 
 template <int KMAX>
-int launch(const int32_t* loads, const int32_t* home, int n, int m, int bonus, int bc, int ic, int32_t* worker_of,
-           int32_t* offsets, int32_t* worklist, int64_t* worker_loads, int* err, cudaStream_t s) {
+int launch(const int32_t* loads, const int32_t* home, int n, const int32_t* n_dev, int m, int bonus, int bc, int ic,
+           int32_t* worker_of, int32_t* offsets, int32_t* worklist, int64_t* worker_loads, int* err,
+           cudaStream_t s) {
   auto kernel = lpt_plan_kernel<KMAX>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(lpt_plan)");
-  kernel<<<1, kThreads, kDynBytes, s>>>(loads, home, n, m, bonus, bc, ic, worker_of, offsets, worklist,
+  kernel<<<1, kThreads, kDynBytes, s>>>(loads, home, n, n_dev, m, bonus, bc, ic, worker_of, offsets, worklist,
                                         worker_loads, err);
   DBSP_LAUNCH_CHECK("launch lpt_plan");
   return DBSP_OK;
@@ -474,10 +477,11 @@ int launch(const int32_t* loads, const int32_t* home, int n, int m, int bonus, i
 
 }  // namespace
 
-extern "C" int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
-                                  int32_t stay_bonus, int32_t block_cost, int32_t item_cost, int32_t* worker_of,
-                                  int32_t* worker_offsets, int32_t* worklist, int64_t* worker_loads,
-                                  void* stream) {
+namespace {
+
+int plan_lpt(const int32_t* loads, const int32_t* home, int n_items, const int32_t* n_dev, int n_workers,
+             int32_t stay_bonus, int32_t block_cost, int32_t item_cost, int32_t* worker_of, int32_t* worker_offsets,
+             int32_t* worklist, int64_t* worker_loads, void* stream) {
   if (n_items < 0 || n_workers < 1 || n_workers > DBSP_MAX_WORKERS || stay_bonus < 0)
     return DBSP_ERR_INVALID_ARG;
   if (block_cost < 1 || block_cost > 65535 || item_cost < 0 || item_cost > (1 << 24)) return DBSP_ERR_INVALID_ARG;
@@ -490,8 +494,8 @@ extern "C" int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int
   int* err = dbsp::error_word(dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int m = n_workers;
-#define DBSP_PLAN_CASE(K)                                                                                 \
-  return launch<K>(loads, home, n_items, m, stay_bonus, block_cost, item_cost, worker_of, worker_offsets, \
+#define DBSP_PLAN_CASE(K)                                                                                        \
+  return launch<K>(loads, home, n_items, n_dev, m, stay_bonus, block_cost, item_cost, worker_of, worker_offsets, \
                    worklist, worker_loads, err, s)
   if (m <= 32) DBSP_PLAN_CASE(1);
   if (m <= 64) DBSP_PLAN_CASE(2);
@@ -502,9 +506,28 @@ extern "C" int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int
 #undef DBSP_PLAN_CASE
 }
 
+}  // namespace
+
+extern "C" int dbsp_plan_lpt_cost(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
+                                  int32_t stay_bonus, int32_t block_cost, int32_t item_cost, int32_t* worker_of,
+                                  int32_t* worker_offsets, int32_t* worklist, int64_t* worker_loads,
+                                  void* stream) {
+  return plan_lpt(loads, home, n_items, nullptr, n_workers, stay_bonus, block_cost, item_cost, worker_of,
+                  worker_offsets, worklist, worker_loads, stream);
+}
+
+extern "C" int dbsp_plan_lpt_cost_n(const int32_t* loads, const int32_t* n_items_dev, int n_items_max,
+                                    int n_workers, int32_t block_cost, int32_t item_cost, int32_t* worker_of,
+                                    int32_t* worker_offsets, int32_t* worklist, int64_t* worker_loads,
+                                    void* stream) {
+  if (!n_items_dev) return DBSP_ERR_INVALID_ARG;
+  return plan_lpt(loads, nullptr, n_items_max, n_items_dev, n_workers, 0, block_cost, item_cost, worker_of,
+                  worker_offsets, worklist, worker_loads, stream);
+}
+
 extern "C" int dbsp_plan_lpt(const int32_t* loads, const int32_t* home, int n_items, int n_workers,
                              int32_t stay_bonus, int32_t* worker_of, int32_t* worker_offsets,
                              int32_t* worklist, int64_t* worker_loads, void* stream) {
-  return dbsp_plan_lpt_cost(loads, home, n_items, n_workers, stay_bonus, 1, 0, worker_of, worker_offsets,
-                            worklist, worker_loads, stream);
+  return plan_lpt(loads, home, n_items, nullptr, n_workers, stay_bonus, 1, 0, worker_of, worker_offsets,
+                  worklist, worker_loads, stream);
 }

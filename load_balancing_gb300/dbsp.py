@@ -38,6 +38,14 @@ _SIGNATURES = {
                                           ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]),
     "dbsp_merge_partials": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp]),
+    "dbsp_plan_lpt_cost_n": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp, _vp,
+                                    _vp]),
+    "dbsp_split_plan": (_i32, [_vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _vp, _vp]),
+    "dbsp_block_sparse_attn_fwd_units": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                                ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp,
+                                                _vp, _vp, _vp, _i32, _vp, _vp]),
+    "dbsp_merge_pieces": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dbsp_device_status": (_i32, [_vp]),
 }
 
@@ -163,6 +171,59 @@ def dbsp_merge_partials(o_parts, m_parts, l_parts, out, lse=None, stream=None):
         _ptr(l_parts, torch.float32, "l_parts"), n, rows, d, _ptr(out, torch.bfloat16, "out"),
         _ptr(lse, torch.float32, "lse", True), _stream(stream))
     _check(st, "dbsp_merge_partials")
+
+
+def dbsp_plan_lpt_cost_n(loads, n_items_dev, n_workers, block_cost, item_cost, worker_of, worker_offsets,
+                         worklist, worker_loads=None, stream=None):
+    """LPT over the first ``n_items_dev[0]`` (device int32) of ``loads`` (capacity loads.numel())."""
+    st = library().dbsp_plan_lpt_cost_n(
+        _ptr(loads, torch.int32, "loads"), _ptr(n_items_dev, torch.int32, "n_items_dev"), loads.numel(),
+        n_workers, int(block_cost), int(item_cost), _ptr(worker_of, torch.int32, "worker_of"),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        _ptr(worker_loads, torch.int64, "worker_loads", True), _stream(stream))
+    _check(st, "dbsp_plan_lpt_cost_n")
+
+
+def dbsp_split_plan(loads, n_workers, max_piece_load, max_pieces, max_slots, unit_item, unit_pk, unit_slot,
+                    unit_load, split_item, split_off, counts, stream=None):
+    """Unit table of heavy items split along their KV blocks (int32 outputs, counts [5])."""
+    st = library().dbsp_split_plan(
+        _ptr(loads, torch.int32, "loads"), loads.numel(), n_workers, int(max_piece_load), int(max_pieces),
+        int(max_slots), _ptr(unit_item, torch.int32, "unit_item"), _ptr(unit_pk, torch.int32, "unit_pk"),
+        _ptr(unit_slot, torch.int32, "unit_slot"), _ptr(unit_load, torch.int32, "unit_load"),
+        _ptr(split_item, torch.int32, "split_item"), _ptr(split_off, torch.int32, "split_off"),
+        _ptr(counts, torch.int32, "counts"), _stream(stream))
+    _check(st, "dbsp_split_plan")
+
+
+def dbsp_block_sparse_attn_fwd_units(q, k, v, mask, block, causal, worker_offsets, worklist, n_workers,
+                                     unit_item, unit_pk, unit_slot, out, lse, o_piece, m_piece, l_piece,
+                                     scale=0.0, cta_timing=None, stream=None):
+    """Attention over a worklist of units: whole items to out/lse, pieces to o/m/l_piece slots."""
+    B, H, S, d = q.shape
+    st = library().dbsp_block_sparse_attn_fwd_units(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+        _ptr(mask, torch.uint8, "mask"), B, H, S, d, block, int(bool(causal)), float(scale),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        n_workers, _ptr(unit_item, torch.int32, "unit_item"), _ptr(unit_pk, torch.int32, "unit_pk"),
+        _ptr(unit_slot, torch.int32, "unit_slot"), unit_item.numel(), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse", True), _ptr(o_piece, torch.float32, "o_piece"),
+        _ptr(m_piece, torch.float32, "m_piece"), _ptr(l_piece, torch.float32, "l_piece"),
+        m_piece.shape[0] if m_piece.dim() == 2 else m_piece.numel() // block,
+        _ptr(cta_timing, torch.int64, "cta_timing", True), _stream(stream))
+    _check(st, "dbsp_block_sparse_attn_fwd_units")
+
+
+def dbsp_merge_pieces(o_piece, m_piece, l_piece, split_item, split_off, counts, out, lse=None, block=128,
+                      stream=None):
+    """Combine the pieces of every split item into out bf16 [B,H,S,d] (and lse fp32 [B,H,S])."""
+    B, H, S, d = out.shape
+    st = library().dbsp_merge_pieces(
+        _ptr(o_piece, torch.float32, "o_piece"), _ptr(m_piece, torch.float32, "m_piece"),
+        _ptr(l_piece, torch.float32, "l_piece"), _ptr(split_item, torch.int32, "split_item"),
+        _ptr(split_off, torch.int32, "split_off"), _ptr(counts, torch.int32, "counts"), B, H, S, d, block,
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse", True), _stream(stream))
+    _check(st, "dbsp_merge_pieces")
 
 
 def dbsp_device_status(stream=None):

@@ -138,3 +138,82 @@ def sharded_attention(q, k, v, shard_masks, block, causal, n_workers, scale=0.0,
     dbsp.dbsp_merge_partials(o_parts.view(n_sh, -1, d), m_parts.view(n_sh, -1), l_parts.view(n_sh, -1),
                              out.view(-1, d), lse.view(-1), stream=stream)
     return out, lse, (o_parts, m_parts, l_parts)
+
+
+@dataclass
+class SplitPlan:
+    """Heavy items split along their KV blocks, and the LPT worklist over the units."""
+    row_loads: torch.Tensor      # int32 [B, H, nQ]
+    col_loads: torch.Tensor      # int32 [B, H, nK]
+    head_loads: torch.Tensor     # int32 [B, H]
+    unit_item: torch.Tensor      # int32 [n_items * max_pieces]
+    unit_pk: torch.Tensor        # int32: j | k << 16
+    unit_slot: torch.Tensor      # int32: partial slot of a piece, -1 for a whole item
+    unit_load: torch.Tensor      # int32: dense blocks of the unit
+    split_item: torch.Tensor     # int32 [n_items]
+    split_off: torch.Tensor      # int32 [n_items + 1]
+    counts: torch.Tensor         # int32 [5]: units, whole items, split items, slots, T
+    worker_of: torch.Tensor      # int32 [n_items * max_pieces], per unit
+    worker_offsets: torch.Tensor  # int32 [n_workers + 1]
+    worklist: torch.Tensor       # int32: unit ids grouped by worker
+    worker_loads: torch.Tensor   # int64 [n_workers]
+    o_piece: torch.Tensor        # fp32 [max_slots, block, d]
+    m_piece: torch.Tensor        # fp32 [max_slots, block]
+    l_piece: torch.Tensor        # fp32 [max_slots, block]
+    n_workers: int
+    max_pieces: int
+    max_slots: int
+
+
+def alloc_split_plan(B, H, nQ, nK, n_workers, block, d, max_pieces, max_slots, device):
+    i32 = dict(dtype=torch.int32, device=device)
+    n = B * H * nQ
+    cap = n * max_pieces
+    return SplitPlan(torch.empty((B, H, nQ), **i32), torch.empty((B, H, nK), **i32), torch.empty((B, H), **i32),
+                     torch.empty(cap, **i32), torch.empty(cap, **i32), torch.empty(cap, **i32),
+                     torch.empty(cap, **i32), torch.empty(n, **i32), torch.empty(n + 1, **i32),
+                     torch.zeros(5, **i32), torch.empty(cap, **i32), torch.empty(n_workers + 1, **i32),
+                     torch.empty(cap, **i32), torch.empty(n_workers, dtype=torch.int64, device=device),
+                     torch.empty((max(max_slots, 1), block, d), dtype=torch.float32, device=device),
+                     torch.empty((max(max_slots, 1), block), dtype=torch.float32, device=device),
+                     torch.empty((max(max_slots, 1), block), dtype=torch.float32, device=device),
+                     n_workers, max_pieces, max_slots)
+
+
+def plan_split(mask, n_workers, block, d, max_piece_load=0, max_pieces=4, max_slots=None, block_cost=1,
+               item_cost=0, out=None, stream=None):
+    """Mask loads -> split plan -> LPT over the units, all on the device (no host sync).
+
+    ``max_piece_load`` T <= 0 selects half the mean load per worker. With that choice a
+    split item of load L > T makes at most ceil(L / T) < 2 L / T pieces, so all pieces
+    together number fewer than 2 total / T <= 4 n_workers: the default ``max_slots``.
+    """
+    B, H, nQ, nK = mask.shape
+    n = B * H * nQ
+    if max_slots is None:
+        max_slots = n * max_pieces if max_piece_load > 0 else min(n * max_pieces, 4 * n_workers)
+    sp = out or alloc_split_plan(B, H, nQ, nK, n_workers, block, d, max_pieces, max_slots, mask.device)
+    dbsp.dbsp_block_mask_loads(mask, sp.row_loads, sp.col_loads, sp.head_loads, stream=stream)
+    dbsp.dbsp_split_plan(sp.row_loads.view(-1), n_workers, max_piece_load, max_pieces, sp.max_slots, sp.unit_item,
+                         sp.unit_pk, sp.unit_slot, sp.unit_load, sp.split_item, sp.split_off, sp.counts,
+                         stream=stream)
+    dbsp.dbsp_plan_lpt_cost_n(sp.unit_load, sp.counts[:1], n_workers, block_cost, item_cost, sp.worker_of,
+                              sp.worker_offsets, sp.worklist, sp.worker_loads, stream=stream)
+    return sp
+
+
+def attention_split(q, k, v, mask, block, causal, sp, out=None, lse=None, scale=0.0, cta_timing=None,
+                    stream=None):
+    """Attention over a split plan: whole items written directly, pieces merged; returns (out, lse)."""
+    B, H, S, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    dbsp.dbsp_block_sparse_attn_fwd_units(q, k, v, mask, block, causal, sp.worker_offsets, sp.worklist,
+                                          sp.n_workers, sp.unit_item, sp.unit_pk, sp.unit_slot, out, lse,
+                                          sp.o_piece, sp.m_piece, sp.l_piece, scale=scale, cta_timing=cta_timing,
+                                          stream=stream)
+    dbsp.dbsp_merge_pieces(sp.o_piece, sp.m_piece, sp.l_piece, sp.split_item, sp.split_off, sp.counts, out, lse,
+                           block=block, stream=stream)
+    return out, lse

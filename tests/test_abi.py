@@ -145,3 +145,39 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(dbsp, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         dbsp.library()
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, 10, 0, 0, 4, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),       # no workers
+    ((FAKE, -1, 4, 0, 4, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),       # negative n
+    ((FAKE, 10, 4, 0, 0, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),       # no pieces
+    ((FAKE, 10, 4, 0, 1025, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),    # too many pieces
+    ((FAKE, 10, 4, 0, 4, -1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),       # negative capacity
+    ((FAKE, 10, 4, 0, 4, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None), 1),       # null counts
+    ((None, 10, 4, 0, 4, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),       # null loads
+    ((FAKE, 3_000_000, 4, 0, 1000, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None), 1),  # n*P overflow
+])
+def test_split_plan_host_validation(built_library, args, expect):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_split_plan(*args) == expect
+
+
+def test_units_and_pieces_host_validation(built_library):
+    from load_balancing_gb300 import dbsp
+
+    lib = dbsp.library()
+    base = [FAKE, FAKE, FAKE, FAKE, 1, 2, 512, 128, 128, 1, 0.0, FAKE, FAKE, 4]
+    tail = [FAKE, FAKE, FAKE, 16, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None, None]
+    assert lib.dbsp_block_sparse_attn_fwd_units(*base, None, *tail[1:]) == 1      # null unit table
+    bad = list(tail)
+    bad[4] = None                                                                   # no final output
+    assert lib.dbsp_block_sparse_attn_fwd_units(*base, *bad) == 1
+    bad = list(tail)
+    bad[9] = -1                                                                     # negative slot capacity
+    assert lib.dbsp_block_sparse_attn_fwd_units(*base, *bad) == 1
+    # the units entry shares the plain entry's shape checks
+    assert lib.dbsp_block_sparse_attn_fwd_units(*base[:7], 96, *base[8:], *tail) == 2  # d = 96
+    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 512, 96, 128, FAKE, None, None) == 1
+    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, None, FAKE, FAKE, 1, 2, 512, 128, 128, FAKE, None, None) == 1
+    assert lib.dbsp_plan_lpt_cost_n(FAKE, None, 10, 4, 1, 0, FAKE, FAKE, FAKE, None, None) == 1
