@@ -594,7 +594,6 @@ def split_study(dev, stream, flush, reps, peaks):
                                       f"Q/K/V bf16 N(0,1)", "dense_blocks": n_dense, "items": w.n_items,
             "n_workers": m, "largest_item": int((mask_np != 0).sum(-1).max()), "mean_per_worker": n_dense / m}
     pb = P.plan(mask, m, stream=stream)
-    sp = P.plan_split(mask, m, w.block, w.d, stream=stream)
 
     def skew():
         tt = timing.view(m, 3).cpu().numpy()
@@ -608,17 +607,37 @@ def split_study(dev, stream, flush, reps, peaks):
     line["whole_lpt"] = {"attn_us": 1e3 * t, "TFLOP/s": flop / t / 1e9, "sm_skew": skew(),
                          "plan_us": 1e3 * _time_ms(lambda: P.plan(mask, m, out=pb, stream=stream), stream, flush,
                                                    reps)}
-    attn_s = lambda: P.attention_split(q, k, v, mask, w.block, w.causal, sp, out=out, lse=lse, cta_timing=timing,
-                                       stream=stream)
-    t_s = _time_ms(attn_s, stream, flush, reps)
-    sk = skew()
-    counts = sp.counts.cpu().numpy().tolist()
-    line["split_lpt"] = {"attn_plus_merge_us": 1e3 * t_s, "TFLOP/s": flop / t_s / 1e9, "sm_skew": sk,
-                         "plan_us": 1e3 * _time_ms(lambda: P.plan_split(mask, m, w.block, w.d, out=sp,
-                                                                        stream=stream), stream, flush, reps),
-                         "units": counts[0], "split_items": counts[2], "pieces": counts[3], "piece_load": counts[4]}
-    line["frac_of_bf16_peak"] = {"whole": flop / t / 1e9 / float(peaks["bf16_tflops"]),
-                                 "split": flop / t_s / 1e9 / float(peaks["bf16_tflops"])}
+    def per_unit_cost(offsets):
+        # busy time against the number of units and blocks per CTA (least squares):
+        # busy ~ a * units + b * blocks
+        tt = timing.view(m, 3).cpu().numpy().astype(np.float64)
+        busy = (tt[:, 1] - tt[:, 0]) / 1e3
+        units = np.diff(offsets.cpu().numpy()).astype(np.float64)
+        coef = np.linalg.lstsq(np.stack([units, tt[:, 2]], 1), busy, rcond=None)[0]
+        return {"us_per_unit": float(coef[0]), "us_per_block": float(coef[1])}
+
+    line["whole_lpt"]["fit"] = per_unit_cost(pb.worker_offsets)
+    mean_t = -(-n_dense // m)
+    line["split_lpt"] = {}
+    for label, t_max in (("half_mean", 0), ("mean", mean_t)):
+        sp = P.plan_split(mask, m, w.block, w.d, max_piece_load=t_max, stream=stream)
+        attn_s = lambda: P.attention_split(q, k, v, mask, w.block, w.causal, sp, out=out, lse=lse,
+                                           cta_timing=timing, stream=stream)
+        t_s = _time_ms(attn_s, stream, flush, reps)
+        sk = skew()
+        fit = per_unit_cost(sp.worker_offsets)
+        counts = sp.counts.cpu().numpy().tolist()
+        t_plan = _time_ms(lambda: P.plan_split(mask, m, w.block, w.d, max_piece_load=t_max, out=sp,
+                                               stream=stream), stream, flush, reps)
+        line["split_lpt"][label] = {"attn_plus_merge_us": 1e3 * t_s, "TFLOP/s": flop / t_s / 1e9, "sm_skew": sk,
+                                    "plan_us": 1e3 * t_plan, "units": counts[0], "split_items": counts[2],
+                                    "pieces": counts[3], "piece_load": counts[4], "fit": fit,
+                                    "planned_max_over_mean": float(sp.worker_loads.max().item() /
+                                                                   sp.worker_loads.float().mean().item()),
+                                    "frac_of_bf16_peak": flop / t_s / 1e9 / float(peaks["bf16_tflops"])}
+    line["whole_lpt"]["planned_max_over_mean"] = float(pb.worker_loads.max().item() /
+                                                       pb.worker_loads.float().mean().item())
+    line["whole_lpt"]["frac_of_bf16_peak"] = flop / t / 1e9 / float(peaks["bf16_tflops"])
     line["device_status"] = dbsp.dbsp_device_status()
     print(json.dumps(line), flush=True)
 

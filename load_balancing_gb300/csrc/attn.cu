@@ -221,7 +221,7 @@ struct RowScan {
 // Producer warp `which` (0: Q and K, 1: V). Both walk the worker's items in list
 // order; producer 0 also publishes every item to the MMA issuer and the softmax
 // warps. `each(col)` is called by lane 0 for the dense blocks of the row, in order.
-template <int BLOCK, int D>
+template <int BLOCK, int D, bool UNITS>
 __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              const AttnParams& p, Ctrl* c, uint8_t* data) {
   using C = Cfg<BLOCK, D>;
@@ -253,7 +253,7 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
     if (idx < end) {
       const int u = __ldg(p.worklist + idx);
       bool valid;
-      if (p.unit_item) {
+      if constexpr (UNITS) {
         valid = u >= 0 && u < p.n_units;
         if (valid) {
           item = __ldg(p.unit_item + u);
@@ -280,7 +280,7 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
     if (item >= 0) {
       kv_row0 = (long long)(item / p.nQ) * p.S;
       limit = rs.limit(item);
-      if (which == 0 || pk > 1) {
+      if (which == 0 || (UNITS && pk > 1)) {
         int L = 0;
         for (int c0 = 0; c0 < limit; c0 += 512) L += __reduce_add_sync(kAll, __popc(rs.bits(item, c0, limit)));
         lo = (int)(((long long)pj * L) / pk);
@@ -293,7 +293,7 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
       // warp writes its rows itself (a piece or partial mode: m = -inf, l = 0, O rows
       // untouched; final mode: O = 0, LSE = -inf).
       const long long row0 = (long long)(item / p.nQ) * p.S + (long long)(item % p.nQ) * BLOCK;
-      if (pslot >= 0) {
+      if (UNITS && pslot >= 0) {
         for (int r = lane; r < BLOCK; r += 32) {
           p.m_piece[(long long)pslot * BLOCK + r] = -INFINITY;
           p.l_piece[(long long)pslot * BLOCK + r] = 0.f;
@@ -361,11 +361,13 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
           while (wb && ok) {
             const int col = c0 + 32 * w + (__ffs(wb) - 1);
             wb &= wb - 1;
-            const int rk = rank++;
-            if (rk < lo) continue;
-            if (rk >= hi) {
-              past = true;
-              break;
+            if constexpr (UNITS) {  // only the unit's dense ranks [lo, hi)
+              const int rk = rank++;
+              if (rk < lo) continue;
+              if (rk >= hi) {
+                past = true;
+                break;
+              }
             }
             const uint32_t s = t_cnt % kstages;
             if (t_cnt >= kstages) {
@@ -385,7 +387,7 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
         }
       }
       ok = __shfl_sync(kAll, ok, 0);
-      past = __shfl_sync(kAll, past, 0);
+      if constexpr (UNITS) past = __shfl_sync(kAll, past, 0);
       __syncwarp();
     }
   }
@@ -516,7 +518,7 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // warp (split 16-lane TMEM shape): thread t < 16 holds columns [0, BLOCK/2) of S and
 // [0, D/2) of O for row t, thread t + 16 the other halves. Row maxima and row sums are
 // combined with one shuffle, so the softmax warps never wait on one another.
-template <int BLOCK, int D>
+template <int BLOCK, int D, bool UNITS>
 __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
   constexpr int CW = BLOCK / 2;  // S columns per thread
   constexpr int DW = D / 2;      // O columns per thread
@@ -535,7 +537,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     const uint32_t slot = items & 1;
     if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
     const int item = c->item_id[slot], n = c->item_n[slot], diag = c->item_diag[slot];
-    const int pslot = c->item_slot[slot];
+    const int pslot = UNITS ? c->item_slot[slot] : -1;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&c->item_empty[slot]));
     ++items;
@@ -640,8 +642,8 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     if (row_ok) {
       const float* of = reinterpret_cast<const float*>(o);
       constexpr float kLn2 = 0.693147180559945309f;
-      if (partial || pslot >= 0) {  // unnormalised partial of a KV shard or of a piece
-        const bool piece = pslot >= 0;
+      if (partial || (UNITS && pslot >= 0)) {  // unnormalised partial of a KV shard or of a piece
+        const bool piece = UNITS && pslot >= 0;
         const long long prow = piece ? (long long)pslot * BLOCK + r : grow;
         const float f = ex2(m_ref - m_true);
         float4* dst = reinterpret_cast<float4*>((piece ? p.o_piece : p.o_part) + prow * D + ch * DW);
@@ -670,7 +672,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
   }
 }
 
-template <int BLOCK, int D>
+template <int BLOCK, int D, bool UNITS>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const AttnParams p) {
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   if (warp < kSoftmaxWarp0) {
     setmaxnreg_dec<kRegsControl>();
     if (warp < 2) {
-      run_producer<BLOCK, D>(warp, &tq, &tk, &tv, p, c, base);
+      run_producer<BLOCK, D, UNITS>(warp, &tq, &tk, &tv, p, c, base);
     } else {
       if (lane == 0) {
         if (warp == kMmaWarp) run_mma_s<BLOCK, D>(p, c, smem_u32(base), tmem);
@@ -730,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
-    run_softmax<BLOCK, D>(p, c, tmem);
+    run_softmax<BLOCK, D, UNITS>(p, c, tmem);
   }
 
   tc_fence_before();
@@ -768,21 +770,30 @@ int encode_map(CUtensorMap* map, const void* ptr, long long rows, int d, int blo
   return r == CUDA_SUCCESS ? DBSP_OK : DBSP_ERR_CUDA;
 }
 
-template <int BLOCK, int D>
-int launch_attn(const void* q, const void* k, const void* v, const AttnParams& p, long long rows,
-                int n_workers, cudaStream_t stream) {
+template <int BLOCK, int D, bool UNITS>
+int launch_attn_t(const void* q, const void* k, const void* v, const AttnParams& p, long long rows,
+                  int n_workers, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   if (encode_map(&tq, q, rows, D, BLOCK) || encode_map(&tk, k, rows, D, BLOCK) ||
       encode_map(&tv, v, rows, D, BLOCK))
     return dbsp::cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
   constexpr size_t smem = smem_bytes<BLOCK, D>();
   static_assert(smem <= 227 * 1024, "shared memory per CTA");
-  auto kernel = attn_fwd_kernel<BLOCK, D>;
+  auto kernel = attn_fwd_kernel<BLOCK, D, UNITS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(attn)");
   kernel<<<n_workers, kThreads, smem, stream>>>(tq, tk, tv, p);
   DBSP_LAUNCH_CHECK("launch attn_fwd");
   return DBSP_OK;
+}
+
+// The unit logic is compiled only into the kernels that take a unit table, so the
+// plain worklist path carries none of it.
+template <int BLOCK, int D>
+int launch_attn(const void* q, const void* k, const void* v, const AttnParams& p, long long rows,
+                int n_workers, cudaStream_t stream) {
+  return p.unit_item ? launch_attn_t<BLOCK, D, true>(q, k, v, p, rows, n_workers, stream)
+                     : launch_attn_t<BLOCK, D, false>(q, k, v, p, rows, n_workers, stream);
 }
 
 }  // namespace
