@@ -507,6 +507,11 @@ def run_suite(args):
                                    "frac_of_bf16_peak": flop / t / 1e9 / float(peaks["bf16_tflops"]),
                                    "sm_skew": float((busy.max() - busy.mean()) / busy.mean()),
                                    "blocks_max_over_mean": float(tt[:, 2].max() / max(1e-9, tt[:, 2].mean()))}
+            if kind == "lpt":  # busy ~ a * items + b * blocks per CTA (least squares)
+                units = np.diff(off.cpu().numpy()).astype(np.float64)
+                coef = np.linalg.lstsq(np.stack([units, tt[:, 2].astype(np.float64)], 1), busy / 1e3,
+                                       rcond=None)[0]
+                line["attn_lpt"]["fit"] = {"us_per_item": float(coef[0]), "us_per_block": float(coef[1])}
         # head-level LPT over a few "virtual GPUs" (db-SP blog, scenario 1): makespan
         # against the lower bound max(ceil(total / m), largest head)
         hl = pb.head_loads.view(-1).contiguous()
