@@ -250,10 +250,6 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
   bool ok = true;
   for (int idx = begin; idx <= end && ok; ++idx) {
     int item = -1, pj = 0, pk = 1, pslot = -1;
-    // the next entry, for the prefetch of its mask row and Q tile behind this item's
-    // first K tile (whole items only; a unit entry would need one more dependent load)
-    const int next_u = (which == 0 && !UNITS && idx + 1 < end) ? __ldg(p.worklist + idx + 1) : -1;
-    bool prefetched = next_u < 0 || next_u >= p.n_items;
     if (idx < end) {
       const int u = __ldg(p.worklist + idx);
       bool valid;
@@ -386,14 +382,6 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
 #pragma unroll
               for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kTileChunk, map, ch * 64, row, f);
               ++t_cnt;
-              if (!prefetched) {  // the next item's mask row and Q tile into L2
-                prefetched = true;
-                const uint8_t* nrow = p.mask + (long long)next_u * p.nK;
-                for (int b0 = 0; b0 < p.nK; b0 += 128) prefetch_l2(nrow + b0);
-                const int nq = (int)((long long)(next_u / p.nQ) * p.S + (long long)(next_u % p.nQ) * BLOCK);
-#pragma unroll
-                for (int ch = 0; ch < D / 64; ++ch) tma_prefetch_2d(tq, ch * 64, nq);
-              }
             }
           }
         }
