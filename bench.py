@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) of one attention launch on this workload, from the ncu capture
 # summarised in profiles/attn_fwd_llm.md, valid only for the kernel source it was taken on.
-NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "76abcb4a83f64004", "bytes": 308.6e6,
+NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "583f1c2b14746797", "bytes": 309.96e6,
                     "source": "profiles/attn_fwd_llm.md"}
 
 
