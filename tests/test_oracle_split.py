@@ -113,3 +113,26 @@ def test_split_attention_equals_unsplit(causal):
             rows = slice(qb * block, (qb + 1) * block)
             np.testing.assert_allclose(o, ref_o[b, h, rows], rtol=0, atol=1e-12)
             np.testing.assert_allclose(lse, ref_lse[b, h, rows], rtol=0, atol=1e-12)
+
+
+def test_automatic_piece_load_bounds_the_slots():
+    """With T = auto_piece_load(total, m), an item of L > T dense blocks makes at most
+    ceil(L / T) < 2 L / T pieces, so all pieces together number fewer than
+    2 total / T <= 4 m: the capacity the split path allocates by default."""
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        m = int(rng.integers(1, 300))
+        n = int(rng.integers(1, 3000))
+        kind = rng.integers(0, 3)
+        if kind == 0:
+            loads = rng.integers(0, 200, n)
+        elif kind == 1:  # a few very heavy items
+            loads = rng.integers(0, 3, n)
+            loads[rng.integers(0, n, 3)] = rng.integers(1000, 100000, 3)
+        else:  # every item just above the automatic T
+            t0 = OS.auto_piece_load(n * 50, m)
+            loads = np.full(n, t0 + 1)
+        total = int(loads.sum())
+        t = OS.auto_piece_load(total, m)
+        tab = OS.split_plan(loads, t, 10**6)
+        assert tab["counts"][3] < 4 * m or total == 0
