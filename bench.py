@@ -572,7 +572,42 @@ def run_suite(args):
         torch.cuda.empty_cache()
     if not args.workloads or "long_causal" in names:
         split_study(dev, stream, flush, reps, peaks)
+    if not args.workloads or "bonus" in names:
+        bonus_study(dev, stream, flush, reps)
     return 0
+
+
+def bonus_study(dev, stream, flush, reps):
+    """Plan reuse across consecutive masks (db-SP blog, scenario 2, third bullet): the
+    next step's mask flips 2 % of the blocks; its plan takes the previous plan as home
+    with a stay bonus. Reported per bonus: the fraction of items kept on their worker,
+    the makespan over the lower bound max(ceil(total / m), largest item), plan time."""
+    import torch
+
+    from load_balancing_gb300 import path as P
+    from load_balancing_gb300 import workloads as W
+
+    m = P.default_workers(dev)
+    for name in ("llm", "video"):
+        w = W.WORKLOADS[name]
+        mask0_np = W.make_mask(w)
+        mask1_np = W.perturb_mask(mask0_np, 0.02, 1, w.causal)
+        mask0 = torch.from_numpy(mask0_np).to(dev)
+        mask1 = torch.from_numpy(mask1_np).to(dev)
+        p0 = P.plan(mask0, m, stream=stream)
+        home = p0.worker_of.clone()
+        loads1 = (mask1_np != 0).sum(-1).reshape(-1)
+        bound = max(-(-int(loads1.sum()) // m), int(loads1.max()))
+        line = {"suite": True, "study": "stay bonus", "workload": name, "flipped_fraction": 0.02,
+                "n_workers": m, "lower_bound": bound, "bonus": {}}
+        for bonus in (0, 1, 2, 4, 8, 16, 32, 1 << 20):
+            p1 = P.plan(mask1, m, home=home, stay_bonus=bonus, stream=stream)
+            stay = float((p1.worker_of == home).float().mean().item())
+            makespan = int(p1.worker_loads.max().item())
+            t = _time_ms(lambda: P.plan(mask1, m, home=home, stay_bonus=bonus, out=p1, stream=stream), stream,
+                         flush, reps)
+            line["bonus"][str(bonus)] = {"stay": stay, "makespan_over_bound": makespan / bound, "plan_us": 1e3 * t}
+        print(json.dumps(line), flush=True)
 
 
 def split_study(dev, stream, flush, reps, peaks):

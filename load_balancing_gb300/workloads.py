@@ -155,6 +155,17 @@ def make_mask(w):
     return np.ascontiguousarray(m, dtype=np.uint8)
 
 
+def perturb_mask(mask, frac, seed, causal):
+    """The next step's mask: every block flipped (dense <-> empty) with probability
+    ``frac``, seeded; blocks above the diagonal stay empty when ``causal``."""
+    rng = np.random.default_rng(seed)
+    flip = rng.random(mask.shape) < frac
+    m = np.where(flip, 1 - (mask != 0), mask != 0).astype(np.uint8)
+    if causal:
+        m = _causal_clip(m)
+    return np.ascontiguousarray(m)
+
+
 def shard_columns(nK, n_shards, layout):
     """KV-block column ids of each shard.
 

@@ -78,3 +78,16 @@ def test_qkv_bf16_values_and_determinism():
     a = W.make_qkv(small)[0]
     b = W.make_qkv(small)[0]
     assert torch.equal(a, b)
+
+
+def test_perturbed_mask():
+    w = W.WORKLOADS["llm"]
+    m0 = W.make_mask(w)
+    m1 = W.perturb_mask(m0, 0.02, 1, w.causal)
+    assert np.array_equal(m1, W.perturb_mask(m0, 0.02, 1, w.causal))  # seeded
+    nq = w.nQ
+    upper = np.triu(np.ones((nq, nq), dtype=bool), 1)
+    assert not m1[..., upper].any()  # causal clip kept
+    lower = ~upper
+    changed = (m0 != m1)[..., lower].mean()
+    assert 0.015 < changed < 0.025
