@@ -187,6 +187,9 @@ def plan_split(mask, n_workers, block, d, max_piece_load=0, max_pieces=4, max_sl
     ``max_piece_load`` T <= 0 selects half the mean load per worker. With that choice a
     split item of load L > T makes at most ceil(L / T) < 2 L / T pieces, so all pieces
     together number fewer than 2 total / T <= 4 n_workers: the default ``max_slots``.
+    With a fixed T the default is the worst case n_items * max_pieces; the piece buffers
+    take max_slots * block * (d + 2) * 4 bytes, so pass a smaller ``max_slots`` for large
+    problems (a plan that needs more pieces reports DBSP_ERR_UNSUPPORTED on the device).
     """
     B, H, nQ, nK = mask.shape
     n = B * H * nQ
