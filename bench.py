@@ -35,10 +35,10 @@ METRIC = "block-sparse attn fwd TFLOP/s on dense blocks, % of bf16 TC peak, SM s
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one attention launch on this workload, from the ncu capture
-# summarised in profiles/attn_fwd_llm.md, valid only for the kernel source it was taken on.
-NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "583f1c2b14746797", "bytes": 309.96e6,
-                    "source": "profiles/attn_fwd_llm.md"}
+# DRAM bytes (read + write) of one attention launch on this workload, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel source it was
+# taken on: any other attn.cu reports null.
+NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "583f1c2b14746797", "bytes": 309.96e6}
 
 
 def attn_traffic():
@@ -75,6 +75,14 @@ MASK_TEXT = {
 def workload_description(w):
     return (f"{w.name}: B={w.B} H={w.H} S={w.S} d={w.d} block={w.block} causal={int(w.causal)}; "
             f"{MASK_TEXT.get(w.name, w.kind)}; Q/K/V bf16 N(0,1)")
+
+
+def bench_config(w, n_workers, n_dense, world=1):
+    """The ``config`` object of the JSON line; both arms print the same one."""
+    return {"workload": workload_description(w), "n_workers": n_workers, "worklist": "LPT",
+            "dense_blocks": n_dense, "items": w.n_items,
+            "l2": "flushed by a 256 MiB write before every timed GPU step (outside the events)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def dense_blocks(mask_np, causal):
@@ -215,6 +223,18 @@ def cpu_baseline(w, mask_np):
 
 
 # ----------------------------------------------------------------------------- reference arm
+def gpu_sm_count(default):
+    """SM count of GPU 0 (the GPU arm's worker count), or ``default`` without a GPU."""
+    try:
+        import torch
+
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return default
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if world > 1 and rank != 0:
@@ -231,7 +251,7 @@ def run_reference(args):
     cores = len(os.sched_getaffinity(0))
     sample_heads = [0, 16]  # one global and one local head per step
     sub_mask = np.ascontiguousarray(mask_np[:, sample_heads])
-    m = 148
+    m = args.workers  # the GPU arm's worker count: one per SM
 
     def step():
         t0 = time.perf_counter()
@@ -251,7 +271,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": workload_description(w)},
+            "data": "synthetic", "config": bench_config(w, m, dense_blocks(mask_np, w.causal), world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "per step: oracle mask loads and textbook LPT over the full workload "
                                        f"({w.n_items} items, m={m}) plus fp64 attention of 2 whole heads "
@@ -389,10 +409,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_description(w), "n_workers": n_workers, "worklist": "LPT (device)",
-                   "dense_blocks": n_dense, "items": w.n_items,
-                   "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(w, n_workers, n_dense, world),
         "attn_tflops": attn_tflops,
         "attn_tflops_fa_convention": flop_fa / attn_avg_s / 1e12,
         "pct_of_bf16_peak": 100.0 * attn_tflops / peak,
@@ -738,6 +755,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dbsp", "reference"], default="dbsp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workers", type=int, default=0,
+                    help="LPT workers of the reference arm (default: the GPU's SM count, else 152)")
     ap.add_argument("--suite", action="store_true", help="one line per workload, every kernel timed alone")
     ap.add_argument("--workloads", default="", help="comma-separated workload names for --suite")
     ap.add_argument("--profile-kernels", action="store_true",
@@ -746,6 +765,8 @@ def main():
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     if args.impl == "reference":
+        if args.workers <= 0:
+            args.workers = gpu_sm_count(152)
         return run_reference(args)
     if args.suite:
         return run_suite(args)

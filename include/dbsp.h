@@ -261,12 +261,16 @@ DBSP_API int dbsp_block_sparse_attn_fwd_units(const void* q, const void* k, cons
  * is empty). Rows of whole items are not touched.
  *
  *   split_item, split_off, counts: as written by dbsp_split_plan (device).
+ *   max_slots  >= 0: capacity of the piece buffers, in slots (as given to
+ *              dbsp_split_plan); no slot at or beyond it, nor beyond counts[3], is read.
  *   out bf16 [B, H, S, d], lse fp32 [B, H, S] or NULL; d in {64, 128}.
- * A split entry out of range sets DBSP_ERR_INVALID_ARG on the device.
+ * A split entry out of range (item, or slots outside [0, min(counts[3], max_slots)))
+ * sets DBSP_ERR_INVALID_ARG on the device and its rows are skipped.
  */
 DBSP_API int dbsp_merge_pieces(const float* o_piece, const float* m_piece, const float* l_piece,
                       const int32_t* split_item, const int32_t* split_off, const int32_t* counts,
-                      int B, int H, int S, int d, int block, void* out, float* lse, void* stream);
+                      int max_slots, int B, int H, int S, int d, int block, void* out, float* lse,
+                      void* stream);
 
 /*
  * Merge of KV-shard partials.  [6D notes §2.1, step 3 and the final division]:

@@ -56,9 +56,9 @@ def needs_build():
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def _compile(src, verbose):
-    obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + ["-c", src, "-o", obj]
+def _compile(src, verbose, out_dir=BUILD_DIR, extra=()):
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -85,6 +85,32 @@ def build(verbose=False):
             if log:
                 print(log)
     return library_path()
+
+
+WAIT_TEST_LIB = os.path.join(BUILD_DIR, "wait_test", "libdbsp_waittest.so")
+
+
+def build_wait_test():
+    """Test-only library: every source compiled with -DDBSP_WAIT_TEST.
+
+    In that build every pipeline wait of the attention kernel gives up after 20 ms,
+    and the V producer of CTA 0 leaves out its first tile (neither its arrival nor its
+    copy is issued), so that a wait runs out and the abort / drain / TMEM-free teardown
+    runs. The product library never contains this code. Returns the path of the .so
+    (under _build/).
+    """
+    out_dir = os.path.dirname(WAIT_TEST_LIB)
+    os.makedirs(out_dir, exist_ok=True)
+    srcs = sources()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
+        objs = [o for o, _ in ex.map(lambda s: _compile(s, False, out_dir, ["-DDBSP_WAIT_TEST"]), srcs)]
+    tmp = WAIT_TEST_LIB + ".tmp"
+    res = subprocess.run([nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs,
+                         capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"link failed (wait test):\n{res.stdout}\n{res.stderr}")
+    os.replace(tmp, WAIT_TEST_LIB)
+    return WAIT_TEST_LIB
 
 
 if __name__ == "__main__":

@@ -74,7 +74,14 @@ constexpr int kVStages = 2;
 // a ring stage is reused after the S (K) or PV (V) that read it completed, tested on the
 // per-S-buffer barriers: a ring may not be deeper than the S buffers
 static_assert(kKStages <= kSBufs && kVStages <= kSBufs, "ring deeper than the S buffers");
+#ifdef DBSP_WAIT_TEST
+// Test build only (never the product library): waits give up after 20 ms, and the V
+// producer of CTA 0 leaves out its first tile (no arrival, no copy), so that the PV
+// issuer's wait for that tile runs out and the whole teardown path runs.
+constexpr uint64_t kWaitLimitNs = 20000000ull;      // 20 ms per wait
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
+#endif
 constexpr uint64_t kDrainLimitNs = 100000000ull;    // 100 ms per teardown wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: P <= 256 between rescales
 
@@ -153,6 +160,13 @@ __device__ __forceinline__ bool wait_bar(Ctrl* c, uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+// Bounded wait taken by every lane of a warp; the warp agrees on the outcome, so that a
+// lane that saw the phase complete never runs ahead of one that saw the abort flag
+// into a warp-collective instruction.
+__device__ __forceinline__ bool warp_wait_bar(Ctrl* c, uint32_t bar, uint32_t parity, int* err) {
+  return __all_sync(0xffffffffu, wait_bar(c, bar, parity, err));
 }
 
 // Teardown wait: ignores the abort flag, short limit, no error on success.
@@ -374,6 +388,12 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
               const uint32_t prev = t_cnt - kstages;
               ok = wait_bar(c, smem_u32(&done[prev % kSBufs]), (prev / kSBufs) & 1, p.err);
             }
+#ifdef DBSP_WAIT_TEST
+            if (ok && which == 1 && blockIdx.x == 0 && t_cnt == 0) {  // the left-out tile
+              ++t_cnt;
+              continue;
+            }
+#endif
             if (ok) {
               const uint32_t f = smem_u32(which == 0 ? &c->k_full[s] : &c->p_full[t_cnt % kSBufs]);
               mbar_arrive_expect_tx(f, C::kTx);
@@ -420,7 +440,8 @@ __device__ void run_mma_s(const AttnParams& p, Ctrl* c, uint32_t data, uint32_t 
     const uint32_t slot = items & 1;
     if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
     const int item = c->item_id[slot], n = c->item_n[slot];
-    ++items;  // the PV issuer, which is behind, releases the slot
+    mbar_arrive(smem_u32(&c->item_empty[slot]));  // every reader of the slot releases it
+    ++items;
     if (item < 0) break;
     if (n == 0) continue;
     const uint32_t qs = qc % kQBufs;
@@ -535,7 +556,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
   bool ok = true;
   while (ok) {
     const uint32_t slot = items & 1;
-    if (!wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
+    if (!warp_wait_bar(c, smem_u32(&c->item_full[slot]), (items >> 1) & 1, p.err)) break;
     const int item = c->item_id[slot], n = c->item_n[slot], diag = c->item_diag[slot];
     const int pslot = UNITS ? c->item_slot[slot] : -1;
     __syncwarp();
@@ -550,7 +571,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     for (int j = 0; j < n; ++j, ++G) {
       const uint32_t b = G % kSBufs, bu = G / kSBufs;
       const uint32_t sbase = lane_base + kSCol + b * 128;
-      if (!wait_bar(c, smem_u32(&c->s_full[b]), bu & 1, p.err)) { ok = false; break; }
+      if (!warp_wait_bar(c, smem_u32(&c->s_full[b]), bu & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[CW];
       if constexpr (CW == 64) tmem_ld64s_wait<CW>(sbase, sr);
@@ -612,7 +633,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
       if (__any_sync(0xffffffffu, rescale)) {
         // O may be touched only once PV of the previous block is complete
         const uint32_t gp = G - 1, pb = gp % kSBufs;
-        if (!wait_bar(c, smem_u32(&c->pv_done[pb]), (gp / kSBufs) & 1, p.err)) { ok = false; break; }
+        if (!warp_wait_bar(c, smem_u32(&c->pv_done[pb]), (gp / kSBufs) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < DW / 32; ++cc) {
@@ -633,7 +654,7 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     // epilogue: wait for the last PV of this item; the next item's first PV waits for
     // these warps' P, which they store only after the reads below
     const uint32_t gl = G - 1;
-    if (!wait_bar(c, smem_u32(&c->pv_done[gl % kSBufs]), (gl / kSBufs) & 1, p.err)) break;
+    if (!warp_wait_bar(c, smem_u32(&c->pv_done[gl % kSBufs]), (gl / kSBufs) & 1, p.err)) break;
     tc_fence_after();
     uint32_t o[DW];
     if constexpr (DW == 64) tmem_ld64s_wait<DW>(lane_base, o);
@@ -697,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&c->item_full[i]), 1);
-      mbar_init(smem_u32(&c->item_empty[i]), 9);  // MMA issuer + 8 softmax warps
+      mbar_init(smem_u32(&c->item_empty[i]), 10);  // both MMA issuers + 8 softmax warps
     }
     mbar_init(smem_u32(&c->drain), 2);  // one commit per MMA issuer
     c->abort_flag = 0;

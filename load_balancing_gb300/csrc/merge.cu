@@ -108,10 +108,11 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
 __global__ void __launch_bounds__(kThreads) merge_pieces_kernel(
     const float* __restrict__ o_piece, const float* __restrict__ m_piece, const float* __restrict__ l_piece,
     const int32_t* __restrict__ split_item, const int32_t* __restrict__ split_off,
-    const int32_t* __restrict__ counts, int n_items, int nQ, int S, int block, int d,
+    const int32_t* __restrict__ counts, int max_slots, int n_items, int nQ, int S, int block, int d,
     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int* err) {
   const int lane = threadIdx.x & 31;
   const int n_split = counts[2];
+  const int n_slots = min(counts[3], max_slots);  // slots that hold pieces, within the buffers
   if (n_split < 0 || n_split > n_items) {
     if (blockIdx.x == 0 && threadIdx.x == 0) dbsp::report(err, DBSP_ERR_INVALID_ARG);
     return;
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) merge_pieces_kernel(
   for (long long row = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); row < rows; row += warps) {
     const int si = (int)(row / block), r = (int)(row - (long long)si * block);
     const int item = split_item[si], s0 = split_off[si], s1 = split_off[si + 1];
-    if (item < 0 || item >= n_items || s0 < 0 || s1 < s0) {
+    if (item < 0 || item >= n_items || s0 < 0 || s1 < s0 || s1 > n_slots) {
       if (lane == 0) dbsp::report(err, DBSP_ERR_INVALID_ARG);
       continue;
     }
@@ -190,8 +191,10 @@ extern "C" int dbsp_merge_partials(const float* o_parts, const float* m_parts, c
 
 extern "C" int dbsp_merge_pieces(const float* o_piece, const float* m_piece, const float* l_piece,
                                  const int32_t* split_item, const int32_t* split_off, const int32_t* counts,
-                                 int B, int H, int S, int d, int block, void* out, float* lse, void* stream) {
+                                 int max_slots, int B, int H, int S, int d, int block, void* out, float* lse,
+                                 void* stream) {
   if (B < 1 || H < 1 || S < 1 || (d != 64 && d != 128) || block < 1 || S % block != 0) return DBSP_ERR_INVALID_ARG;
+  if (max_slots < 0) return DBSP_ERR_INVALID_ARG;
   if (!o_piece || !m_piece || !l_piece || !split_item || !split_off || !counts || !out) return DBSP_ERR_INVALID_ARG;
   if (!dbsp::aligned(o_piece, 16) || !dbsp::aligned(out, 8) || !dbsp::aligned(m_piece, 4) ||
       !dbsp::aligned(l_piece, 4) || (lse && !dbsp::aligned(lse, 4)))
@@ -204,7 +207,7 @@ extern "C" int dbsp_merge_pieces(const float* o_piece, const float* m_piece, con
   const long long want = (n_items * block + (kThreads / 32) - 1) / (kThreads / 32);
   const int blocks = (int)std::max<long long>(1, std::min<long long>(want, (long long)dbsp::sm_count(dev) * 8));
   merge_pieces_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      o_piece, m_piece, l_piece, split_item, split_off, counts, (int)n_items, S / block, S, block, d,
+      o_piece, m_piece, l_piece, split_item, split_off, counts, max_slots, (int)n_items, S / block, S, block, d,
       static_cast<__nv_bfloat16*>(out), lse, dbsp::error_word(dev));
   DBSP_LAUNCH_CHECK("launch merge_pieces");
   return DBSP_OK;

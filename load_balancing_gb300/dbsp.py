@@ -45,7 +45,7 @@ _SIGNATURES = {
     "dbsp_block_sparse_attn_fwd_units": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                                 ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp,
                                                 _vp, _vp, _vp, _i32, _vp, _vp]),
-    "dbsp_merge_pieces": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "dbsp_merge_pieces": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dbsp_device_status": (_i32, [_vp]),
 }
 
@@ -59,6 +59,16 @@ class DbspError(RuntimeError):
         super().__init__(f"{where}: status {status} ({msg}){': ' + extra if extra else ''}")
 
 
+def open_library(path):
+    """Loads a build of the library at ``path`` and declares every entry point's types."""
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def library():
     """The loaded libdbsp.so (raises if it was never built)."""
     global _lib
@@ -66,12 +76,7 @@ def library():
         if not os.path.exists(_LIB_PATH):
             raise RuntimeError(f"libdbsp.so is not built ({_LIB_PATH}); run "
                                "load_balancing_gb300.build.build() or __graft_entry__.build()")
-        lib = ctypes.CDLL(_LIB_PATH)
-        for name, (res, args) in _SIGNATURES.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
+        _lib = open_library(_LIB_PATH)
     return _lib
 
 
@@ -216,12 +221,16 @@ def dbsp_block_sparse_attn_fwd_units(q, k, v, mask, block, causal, worker_offset
 
 def dbsp_merge_pieces(o_piece, m_piece, l_piece, split_item, split_off, counts, out, lse=None, block=128,
                       stream=None):
-    """Combine the pieces of every split item into out bf16 [B,H,S,d] (and lse fp32 [B,H,S])."""
+    """Combine the pieces of every split item into out bf16 [B,H,S,d] (and lse fp32 [B,H,S]).
+
+    The piece buffers' capacity (slots) is taken from ``m_piece`` ([max_slots, block])."""
     B, H, S, d = out.shape
+    max_slots = m_piece.shape[0] if m_piece.dim() == 2 else m_piece.numel() // block
     st = library().dbsp_merge_pieces(
         _ptr(o_piece, torch.float32, "o_piece"), _ptr(m_piece, torch.float32, "m_piece"),
         _ptr(l_piece, torch.float32, "l_piece"), _ptr(split_item, torch.int32, "split_item"),
-        _ptr(split_off, torch.int32, "split_off"), _ptr(counts, torch.int32, "counts"), B, H, S, d, block,
+        _ptr(split_off, torch.int32, "split_off"), _ptr(counts, torch.int32, "counts"), max_slots, B, H, S, d,
+        block,
         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse", True), _stream(stream))
     _check(st, "dbsp_merge_pieces")
 

@@ -221,3 +221,18 @@ def make_qkv(w, device="cpu"):
     shape = (w.B, w.H, w.S, w.d)
     return tuple(torch.randn(shape, generator=g, device=device, dtype=torch.float32)
                  .to(torch.bfloat16) for _ in range(3))
+
+
+def ramp_key_blocks(k, block, step):
+    """Keys of KV-block j multiplied by (1 + step * j), rounded to bf16 (RNE).
+
+    Later KV-blocks then score higher, so a query row's running maximum keeps growing
+    from one dense block to the next: inputs that drive the online softmax through its
+    rescaling step. ``k`` is a bf16 tensor [B, H, S, d]; the result is a new one.
+    """
+    import torch
+
+    S = k.shape[2]
+    factor = 1.0 + step * (torch.arange(S, device=k.device, dtype=torch.float32) // block)
+    return (k.float() * factor.view(1, 1, S, 1)).to(torch.bfloat16)
+

@@ -82,6 +82,37 @@ def attention_item(q, k, v, mask, b, h, qb, block, causal, scale=None):
     return softmax_rows(q[b, h, rows], k[b, h], v[b, h], allowed, scale)
 
 
+def admissible_key_positions(mask_row, block, qb, causal):
+    """Key positions of the dense KV-blocks of one mask row, ascending, cut at the last
+    query position of Q-block ``qb`` when causal (later keys are admissible to no row
+    of the block)."""
+    cols = np.flatnonzero(np.asarray(mask_row) != 0)
+    pos = (cols[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+    if causal:
+        pos = pos[pos <= (qb + 1) * block - 1]
+    return pos
+
+
+def attention_item_keys(q_rows, k_head, v_head, mask_row, block, qb, causal, scale=None):
+    """One item (the ``block`` query rows of Q-block qb), evaluated over its admissible
+    keys only: the same masked softmax as ``attention_item``, whose excluded keys carry
+    weight exp(-inf) = 0, written as a sum over the admissible set itself. Used where
+    the sequence is long and the row sparse.
+
+    q_rows [block, d]; k_head, v_head [S, d] of the item's head; mask_row [nK].
+    Returns the dict of ``softmax_rows``.
+    """
+    d = q_rows.shape[-1]
+    if scale is None:
+        scale = default_scale(d)
+    pos = admissible_key_positions(mask_row, block, qb, causal)
+    allowed = np.ones((block, pos.size), dtype=bool)
+    if causal:
+        q_pos = qb * block + np.arange(block)
+        allowed &= pos[None, :] <= q_pos[:, None]
+    return softmax_rows(q_rows, np.asarray(k_head)[pos], np.asarray(v_head)[pos], allowed, scale)
+
+
 def attention_head(q, k, v, mask, b, h, block, causal, scale=None):
     """All query rows of head (b, h), one Q-block at a time.
 

@@ -66,3 +66,22 @@ def sample_items(mask_np, n_random, n_heavy, seed, whole_heads=()):
         base = (b * H + h) * nQ
         items |= set(range(base, base + nQ))
     return sorted(items)
+
+
+def check_items(w, mask_np, q, k, v, out, lse, items, scale=None):
+    """Sampled parity: every item of ``items`` against the oracle over its admissible
+    keys, copying each head's K and V to the host once."""
+    by_head = {}
+    for item in items:
+        bh, qb = divmod(int(item), w.nQ)
+        by_head.setdefault(bh, []).append(qb)
+    for bh, qbs in sorted(by_head.items()):
+        b, h = divmod(bh, w.H)
+        kh, vh = to64(k[b, h]), to64(v[b, h])
+        for qb in qbs:
+            rows = slice(qb * w.block, (qb + 1) * w.block)
+            r = A.attention_item_keys(to64(q[b, h, rows]), kh, vh, mask_np[b, h, qb], w.block, qb, w.causal,
+                                      scale)
+            assert_rows_close(to64(out[b, h, rows]), r["o"], to64(lse[b, h, rows]), r["lse"],
+                              what=f"{w.name} item {bh * w.nQ + qb}")
+

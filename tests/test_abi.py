@@ -178,6 +178,8 @@ def test_units_and_pieces_host_validation(built_library):
     assert lib.dbsp_block_sparse_attn_fwd_units(*base, *bad) == 1
     # the units entry shares the plain entry's shape checks
     assert lib.dbsp_block_sparse_attn_fwd_units(*base[:7], 96, *base[8:], *tail) == 2  # d = 96
-    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 512, 96, 128, FAKE, None, None) == 1
-    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, None, FAKE, FAKE, 1, 2, 512, 128, 128, FAKE, None, None) == 1
+    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 1, 2, 512, 96, 128, FAKE, None, None) == 1
+    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, None, FAKE, FAKE, 8, 1, 2, 512, 128, 128, FAKE, None, None) == 1
+    assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 2, 512, 128, 128, FAKE, None,
+                                 None) == 1  # negative slot capacity
     assert lib.dbsp_plan_lpt_cost_n(FAKE, None, 10, 4, 1, 0, FAKE, FAKE, FAKE, None, None) == 1

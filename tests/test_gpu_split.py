@@ -165,6 +165,15 @@ def test_hand_made_units_with_empty_pieces(built_library, cuda_device):
     dbsp.dbsp_block_sparse_attn_fwd_units(qd, kd, vd, mask, block, causal, off, wl, m, i32(unit_item),
                                           i32(unit_pk), i32(bad_slot), out, lse, o_piece, m_piece, l_piece)
     assert dbsp.dbsp_device_status() == dbsp.DBSP_ERR_INVALID_ARG
+    # slots beyond the piece buffers' capacity (or beyond counts[3]) are reported, not read
+    bad_off = list(split_off)
+    bad_off[-1] = slots + 3
+    bad_counts = i32([n_units, 0, len(split_item), slots + 3, 1])
+    dbsp.dbsp_merge_pieces(o_piece, m_piece, l_piece, i32(split_item), i32(bad_off), bad_counts, out, lse,
+                           block=block)
+    assert dbsp.dbsp_device_status() == dbsp.DBSP_ERR_INVALID_ARG
+    dbsp.dbsp_merge_pieces(o_piece, m_piece, l_piece, i32(split_item), i32(bad_off), counts, out, lse, block=block)
+    assert dbsp.dbsp_device_status() == dbsp.DBSP_ERR_INVALID_ARG
 
 
 def test_long_causal_heads_sampled(built_library, cuda_device):

@@ -117,3 +117,32 @@ def test_permuting_heads_permutes_outputs():
     op, lp = A.attention(q[:, perm], k[:, perm], v[:, perm], mask[:, perm], blk, False)
     np.testing.assert_array_equal(op, o[:, perm])
     np.testing.assert_array_equal(lp, lse[:, perm])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_admissible_key_item_matches_sdpa(causal):
+    """The long-sequence form (sum over the admissible keys only) against torch SDPA with
+    the element mask, including a row with no dense block and, when causal, a row whose
+    only blocks lie above the diagonal."""
+    B, H, S, d, blk = 1, 2, 256, 16, 32
+    nQ = S // blk
+    q, k, v = (_rand((B, H, S, d), s) for s in (31, 32, 33))
+    rng = np.random.default_rng(34)
+    mask = (rng.random((B, H, nQ, nQ)) < 0.3).astype(np.uint8)
+    mask[0, 0, 3] = 0                 # no dense block at all
+    mask[0, 1, 2] = 0
+    mask[0, 1, 2, 5:] = 1             # only blocks above the diagonal (empty when causal)
+    el = np.repeat(np.repeat(mask != 0, blk, axis=2), blk, axis=3)
+    if causal:
+        el &= np.tril(np.ones((S, S), bool))
+    for h in range(H):
+        for qb in range(nQ):
+            rows = slice(qb * blk, (qb + 1) * blk)
+            r = A.attention_item_keys(q[0, h, rows], k[0, h], v[0, h], mask[0, h, qb], blk, qb, causal)
+            live = el[0, h, rows].any(-1)
+            if live.any():
+                ref = _sdpa(q[0, h, rows][live][None], k[0, h][None], v[0, h][None],
+                            attn_mask=el[0, h, rows][live][None])[0]
+                np.testing.assert_allclose(r["o"][live], ref, rtol=0, atol=1e-12)
+            assert (r["o"][~live] == 0).all() and (r["lse"][~live] == -np.inf).all()
+            assert (r["m"][~live] == -np.inf).all() and (r["l"][~live] == 0).all()
