@@ -272,6 +272,39 @@ DBSP_API int dbsp_merge_pieces(const float* o_piece, const float* m_piece, const
                       int max_slots, int B, int H, int S, int d, int block, void* out, float* lse,
                       void* stream);
 
+/* Size of the static piece scratch of dbsp_block_sparse_attn_fwd_split_noalloc. */
+#define DBSP_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Split attention that allocates nothing.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot allocate device memory where they
+ * run attention, such as a serving runtime whose memory pool is fixed up front, or a
+ * host thread that may not call cudaMalloc (it synchronises the device). It runs
+ * dbsp_block_sparse_attn_fwd_units and then dbsp_merge_pieces, with the pieces' fp32
+ * O, m and l kept in a static device array of DBSP_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * that every GPU loading the library holds until the process exits, instead of
+ * buffers passed by the caller. Inputs and outputs are still the caller's:
+ *
+ *   every argument as in dbsp_block_sparse_attn_fwd_units (final mode) and
+ *   dbsp_merge_pieces; max_slots is the piece capacity given to dbsp_split_plan.
+ * Limit: max_slots * block * (d + 2) * 4 bytes must not exceed
+ * DBSP_NOALLOC_SCRATCH_BYTES (e.g. 252 slots at block = d = 128), else the call
+ * returns DBSP_ERR_INVALID_ARG before touching the GPU.
+ * The first call on a device, with that device current, looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it: make that first call before any
+ * stream capture. No part of the scratch needs to start at zero: every piece writes
+ * its m and l, and O is read only where l > 0. All calls share the one array and it
+ * keeps the last call's contents, so calls that overlap on the GPU (e.g. on two
+ * streams) race: order them on one stream or with events. Never calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ */
+DBSP_API int dbsp_block_sparse_attn_fwd_split_noalloc(
+    const void* q, const void* k, const void* v, const uint8_t* mask, int B, int H, int S, int d, int block,
+    int causal, float scale, const int32_t* worker_offsets, const int32_t* worklist, int n_workers,
+    const int32_t* unit_item, const int32_t* unit_pk, const int32_t* unit_slot, int n_units,
+    const int32_t* split_item, const int32_t* split_off, const int32_t* counts, int max_slots, void* out,
+    float* lse, int64_t* cta_timing, void* stream);
+
 /*
  * Merge of KV-shard partials.  [6D notes §2.1, step 3 and the final division]:
  * m* = max_k m_k, l = sum_k exp(m_k - m*) l_k, O = sum_k exp(m_k - m*) O_k / l.

@@ -47,7 +47,11 @@ _SIGNATURES = {
                                                 _vp, _vp, _vp, _i32, _vp, _vp]),
     "dbsp_merge_pieces": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dbsp_device_status": (_i32, [_vp]),
+    "dbsp_block_sparse_attn_fwd_split_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                                        ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp,
+                                                        _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
 }
+DBSP_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class DbspError(RuntimeError):
@@ -233,6 +237,29 @@ def dbsp_merge_pieces(o_piece, m_piece, l_piece, split_item, split_off, counts, 
         block,
         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse", True), _stream(stream))
     _check(st, "dbsp_merge_pieces")
+
+
+def dbsp_block_sparse_attn_fwd_split_noalloc(q, k, v, mask, block, causal, worker_offsets, worklist, n_workers,
+                                             unit_item, unit_pk, unit_slot, split_item, split_off, counts,
+                                             max_slots, out, lse=None, scale=0.0, cta_timing=None, stream=None):
+    """Split attention (units, then the piece merge) with the pieces in the library's static
+    device scratch: nothing is allocated. ``max_slots`` is the piece capacity of the split
+    plan; max_slots * block * (d + 2) * 4 bytes must fit DBSP_NOALLOC_SCRATCH_BYTES."""
+    B, H, S, d = q.shape
+    need = max_slots * block * (d + 2) * 4
+    if need > DBSP_NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"max_slots={max_slots} needs {need} bytes of piece scratch; the static scratch holds "
+                         f"{DBSP_NOALLOC_SCRATCH_BYTES}")
+    st = library().dbsp_block_sparse_attn_fwd_split_noalloc(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+        _ptr(mask, torch.uint8, "mask"), B, H, S, d, block, int(bool(causal)), float(scale),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        n_workers, _ptr(unit_item, torch.int32, "unit_item"), _ptr(unit_pk, torch.int32, "unit_pk"),
+        _ptr(unit_slot, torch.int32, "unit_slot"), unit_item.numel(), _ptr(split_item, torch.int32, "split_item"),
+        _ptr(split_off, torch.int32, "split_off"), _ptr(counts, torch.int32, "counts"), int(max_slots),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse", True),
+        _ptr(cta_timing, torch.int64, "cta_timing", True), _stream(stream))
+    _check(st, "dbsp_block_sparse_attn_fwd_split_noalloc")
 
 
 def dbsp_device_status(stream=None):
