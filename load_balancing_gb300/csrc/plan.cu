@@ -51,13 +51,24 @@ constexpr long long kKeyNone = LLONG_MAX;
 
 constexpr size_t kStagedBytes = 2ull * kStagedMaxItems + 4ull * (kStagedMaxLoad + 2) + 4ull * 8 * (kStagedMaxLoad + 1);
 constexpr size_t kGlobalBytes = 4ull * (kMaxLoadCounting + 2 > kMaxItemsCompare ? kMaxLoadCounting + 2 : kMaxItemsCompare);
-constexpr size_t kDynBytes = kStagedBytes > kGlobalBytes ? kStagedBytes : kGlobalBytes;
+constexpr size_t kDynBytes0 = kStagedBytes > kGlobalBytes ? kStagedBytes : kGlobalBytes;
 
 struct PlanShared {
   int min_load, max_load, bad_home;
   unsigned long long total_load;
   int scan[kThreads / 32 + 1];
 };
+
+// offset of the bucket ring in the dynamic buffer: past the staged order and its cursor
+constexpr size_t kRingOff = (2ull * kStagedMaxItems + 4ull * (kStagedMaxLoad + 2) + 15) / 16 * 16;
+constexpr int kRingWordsMax = 10240;  // bucket words R * ceil(m / 32)
+constexpr int kRingMax = 4096;        // buckets R
+constexpr size_t kPreOff = kRingOff + 4ull * kRingWordsMax;   // scan of the bucket counts
+constexpr size_t kCntOff = kPreOff + 4ull * kRingMax;         // bucket counts
+constexpr size_t kLwOff = kCntOff + 4ull * kRingMax;          // stored load of each worker
+constexpr size_t kAOff = kLwOff + 4ull * DBSP_MAX_WORKERS;    // sorted keys
+constexpr size_t kRingEnd = kAOff + 8ull * DBSP_MAX_WORKERS;
+constexpr size_t kDynBytes = kDynBytes0 > kRingEnd ? kDynBytes0 : kRingEnd;
 
 // Exclusive scan over `n` ints in shared memory `a` (in place). All threads call it.
 __device__ void block_exclusive_scan(int* a, int n, int* warp_sums) {
@@ -232,6 +243,230 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
     }
   }
   for (int j = tid; j < m; j += kThreads) final_load[A[j] & (K)kWorkerMask] = (long long)(A[j] >> kWorkerBits);
+}
+
+// Phase 2 without a bonus when the planning loads are small: sorted keys, rebuilt by a
+// counting sort over a ring of load buckets.
+//
+// A holds the workers' keys (load << 11 | worker) in ascending order. A batch takes
+// the next items s, s+1, ... in the stable order: item s + j goes to worker A[j] for
+// every j below bp = #{j : A[j] < A[0] + W(s + j)} (W the item's planning load, shifted
+// like the keys). That is exactly the one-at-a-time greedy: A[j] - W(s + j) grows with
+// j (keys ascend, loads descend), so the predicate holds for j < bp only, and when item
+// s + j is placed every earlier pick already carries A[i] + W(s + i) >= A[0] + W(s + j)
+// > A[j] while the later keys are larger, so A[j] is the minimum. A batch may span runs
+// of different loads. Two shortcuts:
+//   * bp == 1: the minimum keeps winning while its key stays below the runner-up's,
+//     q = ceil((A[1] - A[0]) / W) picks within the run;
+//   * bp == m with m or more items of one load left in the run: every later round of m
+//     items keeps the same order, so floor(r / m) whole rounds are placed at once and
+//     every load grows by the same amount (kept aside as a shift).
+// After a batch the picked workers move up in a ring of load buckets (bucket L mod R
+// holds, as a bitmask, the workers whose stored load is L; R a power of two >= 2 wmax +
+// 1, since every load stays within [L0, L0 + 2 wmax] of the minimum L0), and A is
+// rebuilt by a counting sort: a worker's new position is the number of workers in
+// lower buckets (an exclusive scan of the bucket counts from L0) plus the workers below
+// it in its own bucket.
+constexpr int kRingWords = kRingWordsMax;  // R * ceil(m / 32) bucket words
+constexpr int kWorkersPerThread = DBSP_MAX_WORKERS / kThreads;
+
+// Returns false (uniformly) when the state is found inconsistent (a batch without a
+// pick, or more batches than items) instead of looping.
+__device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads, const uint16_t* __restrict__ sorted,
+                                              const int* bin_end, int nbins, int max_load, int n, int m, int bc,
+                                              int ic, int R, uint32_t* bkt, int* pre, int* bcnt, int* Lw,
+                                              unsigned long long* A, int* counts, long long* final_load,
+                                              int32_t* __restrict__ worker_of, int* red) {
+  constexpr int kW = kThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (m == 1) {  // one worker takes every item, in order
+    for (int t = tid; t < n; t += kThreads) worker_of[sorted[t]] = m * t;
+    long long tot = 0;
+    for (int t = tid; t < n; t += kThreads) tot += (long long)__ldg(loads + sorted[t]) * bc + ic;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane == 0) reinterpret_cast<long long*>(A)[warp] = tot;
+    __syncthreads();
+    if (tid == 0) {
+      long long sum = 0;
+      for (int q = 0; q < kW; ++q) sum += reinterpret_cast<long long*>(A)[q];
+      final_load[0] = sum;
+      counts[0] = n;
+    }
+    __syncthreads();
+    return true;
+  }
+  const int WPB = (m + 31) >> 5;
+  const int rmask = R - 1;
+  for (int j = tid; j < R * WPB; j += kThreads) {
+    uint32_t v = 0;
+    if (j < WPB) {  // bucket 0: every worker
+      const int lo = j * 32;
+      v = m - lo >= 32 ? 0xffffffffu : ((1u << (m - lo)) - 1u);
+    }
+    bkt[j] = v;
+  }
+  for (int j = tid; j < R; j += kThreads) bcnt[j] = j == 0 ? m : 0;
+  for (int j = tid; j < m; j += kThreads) {
+    Lw[j] = 0;
+    counts[j] = 0;
+    A[j] = (unsigned long long)j;
+  }
+  __syncthreads();
+  int L0 = 0;           // stored load of A[0]
+  long long shift = 0;  // load added to every worker by whole rounds
+  int s = 0, bin = 0;
+  long long batches = 0;
+  const long long max_batches = (long long)n + 8;
+  // block-wide sum of one int per thread (uses red; synchronises)
+  auto block_sum = [&](int x) {
+    x = __reduce_add_sync(0xffffffffu, x);
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    int t = 0;
+#pragma unroll
+    for (int q = 0; q < kW; ++q) t += red[q];
+    return t;
+  };
+  while (s < n) {
+    if (++batches > max_batches) return false;
+    while (bin < nbins && bin_end[bin] <= s) ++bin;  // the run that holds item s
+    const int run_end = bin_end[bin];
+    const int ws = (max_load - bin) * bc + ic;       // planning load of item s
+    const unsigned long long key0 = A[0];
+    const int p0 = (int)(key0 & kWorkerMask);
+    if (ws == 0) {  // zero loads never change a key: the rest goes to the minimum
+      const int c0 = counts[p0];
+      for (int t = tid; t < n - s; t += kThreads) worker_of[sorted[s + t]] = p0 + m * (c0 + t);
+      __syncthreads();
+      if (tid == 0) counts[p0] = c0 + (n - s);
+      s = n;
+      break;
+    }
+    // ---- bp: the positions j whose key is below A[0] + W(s + j)
+    const int cap = min(m, n - s);
+    int wj[kWorkersPerThread];
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < kWorkersPerThread; ++k) {
+      const int j = tid + k * kThreads;
+      wj[k] = 0;
+      if (j < cap) {
+        wj[k] = __ldg(loads + sorted[s + j]) * bc + ic;
+        c += A[j] < key0 + ((unsigned long long)wj[k] << kWorkerBits);
+      }
+    }
+    const int bp = block_sum(c);
+    if (bp < 1) return false;
+    if (bp == 1) {
+      // ---- the minimum alone: it keeps winning while its key stays below the runner-up
+      const unsigned long long W = (unsigned long long)ws << kWorkerBits;
+      const int r = run_end - s;
+      const int q = m == 1 ? r : (int)min((unsigned long long)r, (A[1] - key0 + W - 1) / W);
+      const int c0 = counts[p0];
+      for (int t = tid; t < q; t += kThreads) worker_of[sorted[s + t]] = p0 + m * (c0 + t);
+      __syncthreads();  // every thread read counts[p0], A[0] and A[1]
+      if (tid == 0) {
+        counts[p0] = c0 + q;
+        const int Lo = Lw[p0], Ln = Lo + q * ws;
+        const uint32_t bit = 1u << (p0 & 31);
+        bkt[(Lo & rmask) * WPB + (p0 >> 5)] &= ~bit;
+        bkt[(Ln & rmask) * WPB + (p0 >> 5)] |= bit;
+        --bcnt[Lo & rmask];
+        ++bcnt[Ln & rmask];
+        Lw[p0] = Ln;
+      }
+      s += q;
+    } else if (bp == m && run_end - s >= m) {
+      // ---- whole rounds of equal loads: the order of A does not change
+      const int F = (run_end - s) / m;
+#pragma unroll
+      for (int k = 0; k < kWorkersPerThread; ++k) {
+        const int j = tid + k * kThreads;
+        if (j < m) {
+          const int p = (int)(A[j] & kWorkerMask);
+          const int c0 = counts[p];
+          for (int f = 0; f < F; ++f) worker_of[sorted[s + f * m + j]] = p + m * (c0 + f);
+          counts[p] = c0 + F;
+        }
+      }
+      shift += (long long)F * ws;
+      s += F * m;
+      __syncthreads();  // A, counts and red are read again by the next batch
+      continue;
+    } else {
+      // ---- a batch: item s + j to worker A[j] for j < bp; each moves up by W(s + j)
+#pragma unroll
+      for (int k = 0; k < kWorkersPerThread; ++k) {
+        const int j = tid + k * kThreads;
+        if (j < bp) {
+          const int p = (int)(A[j] & kWorkerMask);
+          const int c0 = counts[p];
+          worker_of[sorted[s + j]] = p + m * c0;
+          counts[p] = c0 + 1;
+          const int Lo = Lw[p], Ln = Lo + wj[k];
+          const uint32_t bit = 1u << (p & 31);
+          atomicAnd(&bkt[(Lo & rmask) * WPB + (p >> 5)], ~bit);
+          atomicOr(&bkt[(Ln & rmask) * WPB + (p >> 5)], bit);
+          atomicSub(&bcnt[Lo & rmask], 1);
+          atomicAdd(&bcnt[Ln & rmask], 1);
+          Lw[p] = Ln;
+        }
+      }
+      s += bp;
+    }
+    __syncthreads();  // the buckets are final for this batch
+    // ---- counting sort: exclusive scan of the bucket counts from L0 over the ring
+    {
+      const int per = (R + kThreads - 1) / kThreads;
+      const int i0 = min(R, tid * per), i1 = min(R, i0 + per);
+      int tot = 0;
+      for (int i = i0; i < i1; ++i) tot += bcnt[(L0 + i) & rmask];
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) red[warp] = incl;
+      __syncthreads();
+      int run = incl - tot;
+#pragma unroll
+      for (int q = 0; q < kW; ++q) run += q < warp ? red[q] : 0;
+      for (int i = i0; i < i1; ++i) {
+        const int t = bcnt[(L0 + i) & rmask];
+        pre[i] = run;
+        run += t;
+      }
+    }
+    __syncthreads();
+    int bad = 0;  // a load outside [L0, L0 + R) or a position outside [0, m): inconsistent state
+#pragma unroll
+    for (int k = 0; k < kWorkersPerThread; ++k) {
+      const int p = tid + k * kThreads;
+      if (p < m) {
+        const int L = Lw[p];
+        if ((unsigned)(L - L0) >= (unsigned)R) {
+          bad = 1;
+          continue;
+        }
+        const uint32_t* wd = bkt + (L & rmask) * WPB;
+        int pos = pre[L - L0];
+        for (int q = 0; q < (p >> 5); ++q) pos += __popc(wd[q]);
+        pos += __popc(wd[p >> 5] & ((1u << (p & 31)) - 1u));
+        if ((unsigned)pos >= (unsigned)m) {
+          bad = 1;
+          continue;
+        }
+        A[pos] = ((unsigned long long)L << kWorkerBits) | (unsigned long long)p;
+      }
+    }
+    if (__syncthreads_or(bad)) return false;
+    L0 = (int)(A[0] >> kWorkerBits);
+  }
+  __syncthreads();
+  for (int j = tid; j < m; j += kThreads) final_load[j] = (long long)Lw[j] + shift;
+  return true;
 }
 
 // Phase 2 with a bonus: one item at a time (one warp).
@@ -430,7 +665,22 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   __syncthreads();
 
   // ---- phase 2: the greedy
-  if (counting && (home == nullptr || bonus == 0)) {
+  const long long wmax = (long long)max_load * bc + ic;  // the largest planning load
+  int ring_R = 2;
+  while (ring_R < 2 * wmax + 1 && ring_R < (1 << 20)) ring_R <<= 1;
+  const int wpb = (m + 31) >> 5;
+  const bool ring = staged && ring_R <= kRingMax && (long long)ring_R * wpb <= kRingWords &&
+                    (long long)n * wmax < (1LL << 31);
+  if (counting && (home == nullptr || bonus == 0) && ring) {
+    if (!greedy_sorted(loads, sorted.smem, bin_end, nbins, max_load, n, m, bc, ic, ring_R,
+                       reinterpret_cast<uint32_t*>(dyn + kRingOff), reinterpret_cast<int*>(dyn + kPreOff),
+                       reinterpret_cast<int*>(dyn + kCntOff), reinterpret_cast<int*>(dyn + kLwOff),
+                       reinterpret_cast<unsigned long long*>(dyn + kAOff), counts, final_load, worker_of, sh.scan)) {
+      if (tid == 0) dbsp::report(err, DBSP_ERR_UNSUPPORTED);
+      for (int p = tid; p <= m; p += kThreads) offsets[p] = 0;
+      return;
+    }
+  } else if (counting && (home == nullptr || bonus == 0)) {
     // LPT keeps every worker within max_load of the average, so the final worker load is
     // below total / m + max_load; 32-bit keys (load < 2^21) halve the shared-memory
     // traffic of the batch merges whenever that bound allows

@@ -190,3 +190,18 @@ def test_item_cost_spreads_empty_items(built_library, cuda_device):
     assert counts[0].max() >= 950  # the zero loads pile onto one worker
     assert counts[1].max() <= 100  # spread over the workers
     assert wloads[1].max() - wloads[1].min() <= 10 * 8 + 1  # planning loads within one item
+
+
+@pytest.mark.parametrize("m,wmaxes", [(1, (0, 1, 2047)), (152, (511, 512, 818, 819, 2047)),
+                                      (1024, (127, 128, 255, 256))])
+def test_bucket_ring_limits(built_library, cuda_device, m, wmaxes):
+    """The load-bucket greedy runs while the ring (2 wmax + 1 buckets of ceil(m / 32)
+    words) and each batch's window fit their shared-memory budgets; instances on both
+    sides of those limits, with long runs, ties and zero loads, give the textbook LPT."""
+    rng = np.random.default_rng(m)
+    for wmax in wmaxes:
+        for n in (m // 2 + 1, 4 * m + 3, 20000):
+            loads = rng.integers(0, wmax + 1, n)
+            loads[rng.random(n) < 0.2] = max(0, wmax // 3)  # a long run of equal loads
+            loads[0] = wmax
+            _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
