@@ -29,7 +29,8 @@
 //            bonus for that choice only, so items go one at a time: every lane
 //            keeps the keys of workers lane, lane+32, ... in registers and the
 //            warp minimum takes two redux.sync (high word, then low word).
-//            worker_of[i] temporarily holds worker + m * (rank within worker);
+//            worker_of[i] temporarily holds worker + cm * (rank within worker), cm = 1024
+//            (or m when ranks could reach 2^21);
 //   phase 3  CSR offsets by a block scan of the per-worker counts, then the
 //            scatter of every item to offsets[worker] + rank.
 // Global working storage is the output arrays only.
@@ -124,7 +125,7 @@ struct Sorted {  // the stable order, staged in shared memory or in the worklist
 // elements per thread, all searches of a batch in parallel.
 template <int KT, typename K>
 __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbins, int max_load, int n, int m,
-                               int bc, int ic, K* A, int* counts, long long* final_load,
+                               int cm, int bc, int ic, K* A, int* counts, long long* final_load,
                                int32_t* __restrict__ worker_of, int* red) {
   constexpr int kW = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -141,7 +142,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
     if (w == 0) {  // zero loads never change a key: they all go to the current minimum
       const int p0 = (int)(A[h] & (K)kWorkerMask);
       const int base = counts[p0];
-      for (int j = tid; j < r; j += kThreads) worker_of[sorted[s + j]] = p0 + m * (base + j);
+      for (int j = tid; j < r; j += kThreads) worker_of[sorted[s + j]] = p0 + cm * (base + j);
       __syncthreads();
       if (tid == 0) counts[p0] = base + r;
       __syncthreads();
@@ -172,7 +173,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
         step = (K)picks * wk;
         p1 = (int)(key0 & (K)kWorkerMask);
         base1 = counts[p1];
-        for (int j = tid; j < picks; j += kThreads) worker_of[sorted[s + j]] = p1 + m * (base1 + j);
+        for (int j = tid; j < picks; j += kThreads) worker_of[sorted[s + j]] = p1 + cm * (base1 + j);
       } else {
         bp = min(b, r);
         picks = bp;
@@ -181,7 +182,7 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
           const int p = (int)(A[phys(j)] & (K)kWorkerMask);
           const int rank = counts[p];
           counts[p] = rank + 1;
-          worker_of[sorted[s + j]] = p + m * rank;
+          worker_of[sorted[s + j]] = p + cm * rank;
         }
       }
       // merge region: new logical positions [b - bp, m) after the head moves by bp;
@@ -273,14 +274,15 @@ constexpr int kWorkersPerThread = DBSP_MAX_WORKERS / kThreads;
 // Returns false (uniformly) when the state is found inconsistent (a batch without a
 // pick, or more batches than items) instead of looping.
 __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads, const uint16_t* __restrict__ sorted,
-                                              const int* bin_end, int nbins, int max_load, int n, int m, int bc,
-                                              int ic, int R, uint32_t* bkt, int* pre, int* bcnt, int* Lw,
+                                              const uint16_t* __restrict__ sload,
+                                              const int* bin_end, int nbins, int max_load, int n, int m, int cm,
+                                              int bc, int ic, int R, uint32_t* bkt, int* pre, int* bcnt, int* Lw,
                                               unsigned long long* A, int* counts, long long* final_load,
                                               int32_t* __restrict__ worker_of, int* red) {
   constexpr int kW = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (m == 1) {  // one worker takes every item, in order
-    for (int t = tid; t < n; t += kThreads) worker_of[sorted[t]] = m * t;
+    for (int t = tid; t < n; t += kThreads) worker_of[sorted[t]] = cm * t;
     long long tot = 0;
     for (int t = tid; t < n; t += kThreads) tot += (long long)__ldg(loads + sorted[t]) * bc + ic;
 #pragma unroll
@@ -337,7 +339,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
     const int p0 = (int)(key0 & kWorkerMask);
     if (ws == 0) {  // zero loads never change a key: the rest goes to the minimum
       const int c0 = counts[p0];
-      for (int t = tid; t < n - s; t += kThreads) worker_of[sorted[s + t]] = p0 + m * (c0 + t);
+      for (int t = tid; t < n - s; t += kThreads) worker_of[sorted[s + t]] = p0 + cm * (c0 + t);
       __syncthreads();
       if (tid == 0) counts[p0] = c0 + (n - s);
       s = n;
@@ -352,7 +354,15 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
       const int j = tid + k * kThreads;
       wj[k] = 0;
       if (j < cap) {
-        wj[k] = __ldg(loads + sorted[s + j]) * bc + ic;
+        int lj;  // the item's load: staged, or that of the run holding position s + j
+        if (sload) {
+          lj = sload[s + j];
+        } else {
+          int b2 = bin;
+          while (bin_end[b2] <= s + j) ++b2;  // (position s + j < n = the last run's end)
+          lj = max_load - b2;
+        }
+        wj[k] = lj * bc + ic;
         c += A[j] < key0 + ((unsigned long long)wj[k] << kWorkerBits);
       }
     }
@@ -364,7 +374,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
       const int r = run_end - s;
       const int q = m == 1 ? r : (int)min((unsigned long long)r, (A[1] - key0 + W - 1) / W);
       const int c0 = counts[p0];
-      for (int t = tid; t < q; t += kThreads) worker_of[sorted[s + t]] = p0 + m * (c0 + t);
+      for (int t = tid; t < q; t += kThreads) worker_of[sorted[s + t]] = p0 + cm * (c0 + t);
       __syncthreads();  // every thread read counts[p0], A[0] and A[1]
       if (tid == 0) {
         counts[p0] = c0 + q;
@@ -386,7 +396,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
         if (j < m) {
           const int p = (int)(A[j] & kWorkerMask);
           const int c0 = counts[p];
-          for (int f = 0; f < F; ++f) worker_of[sorted[s + f * m + j]] = p + m * (c0 + f);
+          for (int f = 0; f < F; ++f) worker_of[sorted[s + f * m + j]] = p + cm * (c0 + f);
           counts[p] = c0 + F;
         }
       }
@@ -402,7 +412,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
         if (j < bp) {
           const int p = (int)(A[j] & kWorkerMask);
           const int c0 = counts[p];
-          worker_of[sorted[s + j]] = p + m * c0;
+          worker_of[sorted[s + j]] = p + cm * c0;
           counts[p] = c0 + 1;
           const int Lo = Lw[p], Ln = Lo + wj[k];
           const uint32_t bit = 1u << (p & 31);
@@ -472,7 +482,8 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
 // Phase 2 with a bonus: one item at a time (one warp).
 template <int KMAX>
 __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t* __restrict__ loads,
-                              const int32_t* __restrict__ home, int bonus, int bc, int ic, int n, int m, int* counts,
+                              const int32_t* __restrict__ home, int bonus, int bc, int ic, int n, int m, int cm,
+                              int* counts,
                               long long* final_load, int32_t* __restrict__ worker_of) {
   const int lane = threadIdx.x & 31;
   long long key[KMAX];
@@ -521,7 +532,7 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
           cnt[q] += me;
           key[q] += me ? ((long long)w << kWorkerBits) : 0;
         }
-        worker_of[i] = p + m * rank;
+        worker_of[i] = p + cm * rank;
         my_min = lane_minimum(key);
       }
     }
@@ -552,11 +563,48 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   __syncthreads();
   int lmin = INT_MAX, lmax = INT_MIN, badh = 0;
   unsigned long long tot = 0;
-  for (int i = tid; i < n; i += kThreads) {
-    const int w = loads[i];
-    lmin = min(lmin, w); lmax = max(lmax, w);
-    tot += (unsigned long long)max(w, 0) * (unsigned long long)bc + (unsigned long long)ic;
-    if (home) { const int h = home[i]; badh |= (h < 0 || h >= m); }
+  constexpr int kU = 8;  // global reads in flight per thread
+  const bool vec4 = ((reinterpret_cast<uintptr_t>(loads) | reinterpret_cast<uintptr_t>(home)) & 15u) == 0;
+  const int n4 = vec4 ? n / 4 : 0;  // items [0, 4 n4) read as int4
+  for (int base = tid; base < n4; base += kU * kThreads) {
+    int4 v[kU], hv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * kThreads;
+      v[u] = i < n4 ? __ldg(reinterpret_cast<const int4*>(loads) + i) : make_int4(0, 0, 0, 0);
+      hv[u] = (home && i < n4) ? __ldg(reinterpret_cast<const int4*>(home) + i) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (base + u * kThreads < n4) {
+        const int w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const int h4[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          lmin = min(lmin, w4[e]); lmax = max(lmax, w4[e]);
+          tot += (unsigned long long)max(w4[e], 0) * (unsigned long long)bc + (unsigned long long)ic;
+          badh |= (h4[e] < 0 || h4[e] >= m);
+        }
+      }
+    }
+  }
+  for (int base = 4 * n4 + tid; base < n; base += kU * kThreads) {
+    int v[kU], hv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * kThreads;
+      v[u] = i < n ? __ldg(loads + i) : 0;
+      hv[u] = (home && i < n) ? __ldg(home + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (base + u * kThreads < n) {
+        const int w = v[u];
+        lmin = min(lmin, w); lmax = max(lmax, w);
+        tot += (unsigned long long)max(w, 0) * (unsigned long long)bc + (unsigned long long)ic;
+        badh |= (hv[u] < 0 || hv[u] >= m);
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
@@ -577,16 +625,21 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     return;
   }
   const int nbins = max_load + 1;
+  // worker_of holds worker + cm * (rank within worker) until the CSR scatter: cm = 1024
+  // (a shift) whenever ranks stay below 2^21, else m
+  const int cm = n < (1 << 21) ? DBSP_MAX_WORKERS : m;
 
   // ---- phase 1: stable order by (load desc, id asc)
   Sorted sorted{nullptr, worklist};
+  const uint16_t* sload = nullptr;  // load of each sorted position (staged, n <= 22528)
   const int* bin_end = nullptr;  // bin_end[b] = one past the last sorted position of bin b
   if (staged) {
     // 8 warps each take a contiguous id segment: per-warp histograms, a scan over
     // (bin, warp), then each warp scatters its segment in id order (stable)
-    const int n_pad = (n + 7) & ~7;
     uint16_t* order = reinterpret_cast<uint16_t*>(dyn);
-    int* cursor = reinterpret_cast<int*>(order + n_pad);  // [nbins + 1]
+    // the order takes bytes [0, 2n); the loads of the sorted positions, when n <= 22528,
+    // [45056, 45056 + 2n); the bin cursor and the per-warp histograms start at 90112
+    int* cursor = reinterpret_cast<int*>(dyn + 2 * kStagedMaxItems);  // [nbins + 1]
     int* whist = cursor + (nbins + 1);                    // [8][nbins]
     const int warp = tid >> 5;
     constexpr int kWarps = kThreads / 32;
@@ -594,7 +647,26 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     const int lo = min(n, warp * seg), hi = min(n, lo + seg);
     for (int b = tid; b < kWarps * nbins; b += kThreads) whist[b] = 0;
     __syncthreads();
-    for (int i = lo + lane; i < hi; i += 32) atomicAdd(&whist[warp * nbins + (max_load - loads[i])], 1);
+    // the segment [lo, hi): its 16-byte-aligned middle as int4, the ends item by item
+    const int vlo = vec4 ? min(hi, (lo + 3) & ~3) : hi, vhi = vec4 ? max(vlo, hi & ~3) : hi;
+    for (int i = lo + lane; i < vlo; i += 32) atomicAdd(&whist[warp * nbins + (max_load - __ldg(loads + i))], 1);
+    for (int i = vhi + lane; i < hi; i += 32) atomicAdd(&whist[warp * nbins + (max_load - __ldg(loads + i))], 1);
+    for (int base = vlo / 4 + lane; base < vhi / 4; base += 32 * kU) {
+      int4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        v[u] = base + 32 * u < vhi / 4 ? __ldg(reinterpret_cast<const int4*>(loads) + base + 32 * u)
+                                       : make_int4(-1, -1, -1, -1);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (v[u].x >= 0) {
+          atomicAdd(&whist[warp * nbins + (max_load - v[u].x)], 1);
+          atomicAdd(&whist[warp * nbins + (max_load - v[u].y)], 1);
+          atomicAdd(&whist[warp * nbins + (max_load - v[u].z)], 1);
+          atomicAdd(&whist[warp * nbins + (max_load - v[u].w)], 1);
+        }
+      }
+    }
     __syncthreads();
     for (int b = tid; b <= nbins; b += kThreads) {
       int t = 0;
@@ -610,19 +682,34 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     }
     __syncthreads();
     int* mine = whist + warp * nbins;
-    for (int base = lo; base < hi; base += 32) {
-      const int i = base + lane;
-      const unsigned active = __ballot_sync(0xffffffffu, i < hi);
-      if (i < hi) {
-        const int bin = max_load - loads[i];
-        const unsigned peers = __match_any_sync(active, bin);
-        const unsigned below = peers & ((1u << lane) - 1);
-        order[mine[bin] + __popc(below)] = (uint16_t)i;
-        __syncwarp(active);
-        if (below == 0) mine[bin] += __popc(peers);
+    // the loads of each sorted position as well, when they fit beside the order
+    uint16_t* sl = n <= kStagedMaxItems / 2 ? reinterpret_cast<uint16_t*>(dyn + kStagedMaxItems) : nullptr;
+    constexpr int kC = 4;  // chunks of 32 whose loads are read ahead
+    for (int base0 = lo; base0 < hi; base0 += 32 * kC) {
+      int v[kC];
+#pragma unroll
+      for (int u = 0; u < kC; ++u) {
+        const int i = base0 + 32 * u + lane;
+        v[u] = i < hi ? __ldg(loads + i) : 0;
       }
-      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < kC; ++u) {
+        const int i = base0 + 32 * u + lane;
+        const unsigned active = __ballot_sync(0xffffffffu, i < hi);
+        if (i < hi) {
+          const int bin = max_load - v[u];
+          const unsigned peers = __match_any_sync(active, bin);
+          const unsigned below = peers & ((1u << lane) - 1);
+          const int pos = mine[bin] + __popc(below);
+          order[pos] = (uint16_t)i;
+          if (sl) sl[pos] = (uint16_t)v[u];
+          __syncwarp(active);
+          if (below == 0) mine[bin] += __popc(peers);
+        }
+        __syncwarp();
+      }
     }
+    sload = sl;
     sorted = Sorted{order, nullptr};
     bin_end = cursor + 1;
   } else if (counting) {
@@ -672,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   const bool ring = staged && ring_R <= kRingMax && (long long)ring_R * wpb <= kRingWords &&
                     (long long)n * wmax < (1LL << 31);
   if (counting && (home == nullptr || bonus == 0) && ring) {
-    if (!greedy_sorted(loads, sorted.smem, bin_end, nbins, max_load, n, m, bc, ic, ring_R,
+    if (!greedy_sorted(loads, sorted.smem, sload, bin_end, nbins, max_load, n, m, cm, bc, ic, ring_R,
                        reinterpret_cast<uint32_t*>(dyn + kRingOff), reinterpret_cast<int*>(dyn + kPreOff),
                        reinterpret_cast<int*>(dyn + kCntOff), reinterpret_cast<int*>(dyn + kLwOff),
                        reinterpret_cast<unsigned long long*>(dyn + kAOff), counts, final_load, worker_of, sh.scan)) {
@@ -687,13 +774,13 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     constexpr int KT = (KMAX * 32 + kThreads - 1) / kThreads;
     const bool key32 = sh.total_load / (unsigned long long)m + (unsigned long long)max_load * bc + ic < (1ull << 20);
     if (key32)
-      greedy_batched<KT, uint32_t>(sorted, bin_end, nbins, max_load, n, m, bc, ic,
+      greedy_batched<KT, uint32_t>(sorted, bin_end, nbins, max_load, n, m, cm, bc, ic,
                                    reinterpret_cast<uint32_t*>(keys[0]), counts, final_load, worker_of, sh.scan);
     else
-      greedy_batched<KT, long long>(sorted, bin_end, nbins, max_load, n, m, bc, ic, keys[0], counts, final_load,
+      greedy_batched<KT, long long>(sorted, bin_end, nbins, max_load, n, m, cm, bc, ic, keys[0], counts, final_load,
                                     worker_of, sh.scan);
   } else if (tid < 32) {
-    greedy_serial<KMAX>(sorted, loads, home, bonus, bc, ic, n, m, counts, final_load, worker_of);
+    greedy_serial<KMAX>(sorted, loads, home, bonus, bc, ic, n, m, cm, counts, final_load, worker_of);
   }
   __syncthreads();
 
@@ -704,11 +791,45 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   for (int p = tid; p <= m; p += kThreads) offsets[p] = counts[p];
   if (worker_loads)
     for (int p = tid; p < m; p += kThreads) worker_loads[p] = final_load[p];
-  for (int i = tid; i < n; i += kThreads) {
-    const int code = worker_of[i];
-    const int p = code % m, rank = code / m;
-    worklist[counts[p] + rank] = i;
-    worker_of[i] = p;
+  const bool wvec = (reinterpret_cast<uintptr_t>(worker_of) & 15u) == 0;
+  const int nw4 = wvec ? n / 4 : 0;
+  for (int base = tid; base < nw4; base += kU * kThreads) {
+    int4 c4[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      c4[u] = base + u * kThreads < nw4 ? reinterpret_cast<const int4*>(worker_of)[base + u * kThreads]
+                                        : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i4 = base + u * kThreads;
+      if (i4 < nw4) {
+        const int cc[4] = {c4[u].x, c4[u].y, c4[u].z, c4[u].w};
+        int pp[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int p = cm == DBSP_MAX_WORKERS ? (cc[e] & (DBSP_MAX_WORKERS - 1)) : cc[e] % m;
+          const int rank = cm == DBSP_MAX_WORKERS ? (cc[e] >> 10) : cc[e] / m;
+          worklist[counts[p] + rank] = 4 * i4 + e;
+          pp[e] = p;
+        }
+        reinterpret_cast<int4*>(worker_of)[i4] = make_int4(pp[0], pp[1], pp[2], pp[3]);
+      }
+    }
+  }
+  for (int base = 4 * nw4 + tid; base < n; base += kU * kThreads) {
+    int code[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) code[u] = base + u * kThreads < n ? worker_of[base + u * kThreads] : 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * kThreads;
+      if (i < n) {
+        const int p = cm == DBSP_MAX_WORKERS ? (code[u] & (DBSP_MAX_WORKERS - 1)) : code[u] % m;
+        const int rank = cm == DBSP_MAX_WORKERS ? (code[u] >> 10) : code[u] / m;
+        worklist[counts[p] + rank] = i;
+        worker_of[i] = p;
+      }
+    }
   }
 }
 
