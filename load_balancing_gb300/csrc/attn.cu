@@ -131,6 +131,7 @@ struct alignas(8) Ctrl {
   uint64_t q_full[kQBufs], q_empty[kQBufs];
   uint64_t k_full[kKStages];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
+  uint64_t epi_full[kQBufs];  // final mode: the 8 softmax warps wrote an item's bf16 output tile
   uint64_t item_full[2], item_empty[2];
   uint64_t drain;
   int item_id[2], item_n[2], item_diag[2], item_slot[2];
@@ -540,7 +541,8 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // [0, D/2) of O for row t, thread t + 16 the other halves. Row maxima and row sums are
 // combined with one shuffle, so the softmax warps never wait on one another.
 template <int BLOCK, int D, bool UNITS>
-__device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
+__device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem, uint32_t data, const CUtensorMap* to) {
+  using C = Cfg<BLOCK, D>;
   constexpr int CW = BLOCK / 2;  // S columns per thread
   constexpr int DW = D / 2;      // O columns per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -660,10 +662,17 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
     if constexpr (DW == 64) tmem_ld64s_wait<DW>(lane_base, o);
     else tmem_ld32s_wait<DW>(lane_base, o);
     tc_fence_before();
+    const uint32_t ii = items - 1;  // this item's place in the worklist; its Q buffer:
+    const uint32_t qs = ii % kQBufs;
+    const uint32_t qbuf = data + qs * C::kQBytes;
+    // final mode: O / l in bf16 goes into the item's Q buffer (its S products are
+    // complete) in the 128-byte-swizzled layout of the output tensor map, and leaves by
+    // one TMA store; partial outputs are written directly
+    const bool tma_out = !partial && !(UNITS && pslot >= 0);
     if (row_ok) {
       const float* of = reinterpret_cast<const float*>(o);
       constexpr float kLn2 = 0.693147180559945309f;
-      if (partial || (UNITS && pslot >= 0)) {  // unnormalised partial of a KV shard or of a piece
+      if (!tma_out) {  // unnormalised partial of a KV shard or of a piece
         const bool piece = UNITS && pslot >= 0;
         const long long prow = piece ? (long long)pslot * BLOCK + r : grow;
         const float f = ex2(m_ref - m_true);
@@ -677,26 +686,44 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem) {
         }
       } else {
         const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * D + ch * DW);
 #pragma unroll
         for (int i = 0; i < DW / 8; ++i) {
-          uint4 v;
-          v.x = pack_bf16(of[8 * i + 0] * inv, of[8 * i + 1] * inv);
-          v.y = pack_bf16(of[8 * i + 2] * inv, of[8 * i + 3] * inv);
-          v.z = pack_bf16(of[8 * i + 4] * inv, of[8 * i + 5] * inv);
-          v.w = pack_bf16(of[8 * i + 6] * inv, of[8 * i + 7] * inv);
-          dst[i] = v;
+          const int col = ch * DW + 8 * i;  // 16 bytes of row r: unit (col % 64) / 8 of chunk col / 64
+          const uint32_t addr =
+              qbuf + (col >> 6) * C::kChunk128 + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4);
+          st_shared_v4(addr, pack_bf16(of[8 * i + 0] * inv, of[8 * i + 1] * inv),
+                       pack_bf16(of[8 * i + 2] * inv, of[8 * i + 3] * inv),
+                       pack_bf16(of[8 * i + 4] * inv, of[8 * i + 5] * inv),
+                       pack_bf16(of[8 * i + 6] * inv, of[8 * i + 7] * inv));
         }
         if (ch == 0 && p.lse) p.lse[grow] = (m_ref + __log2f(l)) * kLn2;
       }
     }
+    // one thread per item (the softmax warps take turns) releases the Q buffer: in final
+    // mode once the output tile has been stored from it
+    // (every item completes one phase of epi_full of its buffer, whatever the mode)
+    const bool releaser = warp == kSoftmaxWarp0 + (int)(ii % 8) && lane == 0;
+    if (tma_out) fence_proxy_async_smem();  // the generic-proxy writes above, before the TMA store
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&c->epi_full[qs]));
+    if (releaser) {
+      if (wait_bar(c, smem_u32(&c->epi_full[qs]), (ii / kQBufs) & 1, p.err) && tma_out) {
+        const int row0 = (int)(bh * p.S + (long long)qb * BLOCK);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) tma_store_2d(to, qbuf + cc * C::kChunk128, cc * 64, row0);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      mbar_arrive(smem_u32(&c->q_empty[qs]));
+    }
   }
+  if (lane == 0) bulk_wait_all();  // the output stores this warp issued are complete
 }
 
 template <int BLOCK, int D, bool UNITS>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-    const __grid_constant__ CUtensorMap tv, const AttnParams p) {
+    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const AttnParams p) {
   using C = Cfg<BLOCK, D>;
   extern __shared__ uint8_t smem_raw[];
   // shared memory: Q buffers | K ring | V ring | control
@@ -708,7 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQBufs; ++i) {
       mbar_init(smem_u32(&c->q_full[i]), 1);
-      mbar_init(smem_u32(&c->q_empty[i]), 1);
+      // the S issuer's commit (its MMAs read the Q tile) and the item's epilogue (in final
+      // mode the output tile passes through this buffer on its way out)
+      mbar_init(smem_u32(&c->q_empty[i]), 2);
+      mbar_init(smem_u32(&c->epi_full[i]), 8);  // 8 softmax warps
     }
     for (int i = 0; i < kKStages; ++i) mbar_init(smem_u32(&c->k_full[i]), 1);
     for (int i = 0; i < kSBufs; ++i) {
@@ -729,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
+    prefetch_tmap(&to);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&c->tmem_base), kTmemCols);
@@ -753,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
-    run_softmax<BLOCK, D, UNITS>(p, c, tmem);
+    run_softmax<BLOCK, D, UNITS>(p, c, tmem, smem_u32(base), &to);
   }
 
   tc_fence_before();
@@ -794,16 +825,19 @@ int encode_map(CUtensorMap* map, const void* ptr, long long rows, int d, int blo
 template <int BLOCK, int D, bool UNITS>
 int launch_attn_t(const void* q, const void* k, const void* v, const AttnParams& p, long long rows,
                   int n_workers, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (encode_map(&tq, q, rows, D, BLOCK) || encode_map(&tk, k, rows, D, BLOCK) ||
       encode_map(&tv, v, rows, D, BLOCK))
     return dbsp::cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  // final mode: the bf16 output tile leaves shared memory by a TMA store (partial mode: unused)
+  if (encode_map(&to, p.out ? static_cast<const void*>(p.out) : q, rows, D, BLOCK))
+    return dbsp::cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(out)");
   constexpr size_t smem = smem_bytes<BLOCK, D>();
   static_assert(smem <= 227 * 1024, "shared memory per CTA");
   auto kernel = attn_fwd_kernel<BLOCK, D, UNITS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(attn)");
-  kernel<<<n_workers, kThreads, smem, stream>>>(tq, tk, tv, p);
+  kernel<<<n_workers, kThreads, smem, stream>>>(tq, tk, tv, to, p);
   DBSP_LAUNCH_CHECK("launch attn_fwd");
   return DBSP_OK;
 }
