@@ -66,9 +66,12 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
   if (r_off < r_step) {
     for (int c = c0; c < cpr; c += c_step) {
       if (VEC == 16) {
-        // per-byte column counters: 4 words of byte-wide counters, flushed every 252 rows;
+        // per-byte column counters: 4 words of byte-wide counters, flushed before they can pass 255;
         // kUnroll rows are loaded before any is counted, so that many loads are in flight
-        constexpr int kUnroll = 4;
+#ifndef DBSP_LOADS_UNROLL
+#define DBSP_LOADS_UNROLL 8
+#endif
+        constexpr int kUnroll = DBSP_LOADS_UNROLL;
         int cols[16];
 #pragma unroll
         for (int b = 0; b < 16; ++b) cols[b] = 0;
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
             }
           }
           pending += kUnroll;
-          if (pending >= 252) {
+          if (pending + kUnroll > 255) {  // the next kUnroll rows could carry a byte counter past 255
 #pragma unroll
             for (int b = 0; b < 16; ++b) cols[b] += (acc[b >> 2] >> (8 * (b & 3))) & 0xff;
             acc[0] = acc[1] = acc[2] = acc[3] = 0;
