@@ -69,8 +69,10 @@ DBSP_API const char* dbsp_last_error_string(void);
  *   row_loads   int32 [B, H, nQ]  out: dense blocks per Q-block row.
  *   col_loads   int32 [B, H, nK]  out: dense blocks per KV-block column.
  *   head_loads  int32 [B, H]      out, may be NULL.
- * Requires B, H, nQ, nK >= 1 and B*H*nQ*nK < 2^31. Output buffers must not
- * overlap the mask. Exact integer results; one kernel launch.
+ * Requires B, H, nQ, nK >= 1 and B*H*nQ*nK < 2^31; nQ > 131072 or nK > 16384
+ * returns DBSP_ERR_UNSUPPORTED. Output buffers must not overlap the mask. Exact
+ * integer results; one kernel launch. A copy of mask rows that does not arrive
+ * within 2 s sets DBSP_ERR_TIMEOUT on the device.
  */
 DBSP_API int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK,
                           int32_t* row_loads, int32_t* col_loads, int32_t* head_loads,

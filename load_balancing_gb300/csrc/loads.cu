@@ -4,26 +4,53 @@
 // blocks in its mask row, a KV-block's load the number in its column; scenario 1
 // balances whole heads, whose load is the head's total.
 //
-// Design: a thread-block cluster of up to 8 CTAs per (b, h) head. Each CTA scans a
-// band of rows with 16-byte vector loads (byte-granular when the row length or
-// the pointer does not allow it). Row loads are exact per CTA and written
-// directly; column partials live in shared memory and are summed by cluster rank
-// 0 through distributed shared memory, so no global scratch or atomics on the
-// outputs are needed and the outputs need no prior zeroing. HBM-bound: every mask
-// byte is read once.
+// Design: a thread-block cluster of up to 8 CTAs per (b, h) head; each CTA counts a
+// band of rows. Row loads are exact per CTA and written directly; column partials
+// live in shared memory and are summed by cluster rank 0 through distributed shared
+// memory, so no global scratch or atomics on the outputs are needed and the outputs
+// need no prior zeroing. HBM-bound: every mask byte is read once.
+//
+// Rows of at most 4096 bytes on a 16-byte aligned mask (every block mask up to 4096
+// KV blocks) take the streaming kernel: one thread moves the band through a ring of
+// four 16 KB shared-memory stages with bulk asynchronous copies, so 64 KB per CTA is
+// in flight without holding it in registers, and all 256 threads count from shared
+// memory. Longer rows use 16-byte register loads, and rows whose length or pointer
+// does not allow 16-byte access are read byte by byte.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace cg = cooperative_groups;
+using namespace dbsp::ptx;
 
 namespace {
 
+#ifndef DBSP_LOADS_MAX_CLUSTER
+#define DBSP_LOADS_MAX_CLUSTER 8
+#endif
 constexpr int kThreads = 256;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = DBSP_LOADS_MAX_CLUSTER;  // CTAs per head (above 8: non-portable clusters)
 constexpr int kMaxCols = 16384;  // column partials in shared memory: 64 KB
+constexpr int kMaxRows = 131072; // row partials of one CTA (1/8 of a head) in shared memory: 64 KB
+#ifndef DBSP_LOADS_STAGE_BYTES
+#define DBSP_LOADS_STAGE_BYTES 16384
+#endif
+#ifndef DBSP_LOADS_STAGES
+#define DBSP_LOADS_STAGES 4
+#endif
+constexpr int kStageBytes = DBSP_LOADS_STAGE_BYTES;  // streaming kernel: one ring stage
+constexpr int kStages = DBSP_LOADS_STAGES;           // streaming kernel: ring depth
+constexpr int kStreamMaxCols = 4096;                 // rows of <= 4096 B: <= 256 units per row
+static_assert(kStageBytes >= kStreamMaxCols, "a stage holds at least one row");
+static_assert(kStages * kStageBytes >= 16384, "the ring holds the column slots (256 units x 16 ints)");
+constexpr int kStageUnits = kStageBytes / (16 * kThreads);  // 16-byte units per thread in a full stage
+static_assert(kStageUnits >= 1 && kStageUnits < 128, "stage size");
+constexpr size_t kStreamMaxSmem = 200 * 1024;       // streaming kernel: dynamic shared memory cap
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s per stage wait
+constexpr uint64_t kDrainLimitNs = 100000000ull;     // 100 ms per teardown wait
 
 // Number of non-zero bytes in a 32-bit word, as 0x01 flags per byte.
 __device__ __forceinline__ uint32_t nonzero_byte_flags(uint32_t x) {
@@ -152,6 +179,222 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
   cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
+// Bounded wait on a stage's phase. Returns false on timeout (reported as
+// DBSP_ERR_TIMEOUT) or when another thread of the CTA has already given up.
+__device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        dbsp::report(err, DBSP_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Streaming variant for nK % 16 == 0, nK <= kStreamMaxCols and a 16-byte aligned mask.
+// Stage i % kStages holds rows [i * chunk_rows, (i + 1) * chunk_rows) of the CTA's band
+// (chunk_rows * nK <= kStageBytes). Thread t owns the 16-byte column unit t % (nK / 16)
+// and, within a stage, every (256 / (nK / 16))-th row from t / (nK / 16); its per-byte
+// column counters therefore stay in registers across the whole band.
+__global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
+    const uint8_t* __restrict__ mask, int nQ, int nK, int rows_per_cta, int chunk_rows,
+    int32_t* __restrict__ row_loads, int32_t* __restrict__ col_loads, int32_t* __restrict__ head_loads,
+    int* err) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  unsigned char* stage = dsm;                                               // [kStages][kStageBytes]
+  int* recv = reinterpret_cast<int*>(dsm + kStages * kStageBytes);          // [n_ranks][slice]
+  int* row_acc = recv + nK + 4 * kMaxCluster;                               // [rows_per_cta]
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ int cta_total;
+  __shared__ int head_part[kMaxCluster];  // rank 0: every rank's total
+  __shared__ volatile int abort_flag;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int n_ranks = static_cast<int>(cluster.num_blocks());
+  const long long head = blockIdx.y;
+  const int row0 = rank * rows_per_cta;
+  const int rows = max(0, min(nQ, row0 + rows_per_cta) - row0);
+  const int n_chunks = (rows + chunk_rows - 1) / chunk_rows;
+  const uint8_t* band = mask + (head * nQ + row0) * (long long)nK;
+  const int tid = threadIdx.x;
+
+  auto issue = [&](int i) {  // chunk i into stage i % kStages (thread 0 only)
+    const int r = i * chunk_rows;
+    const uint32_t bytes = static_cast<uint32_t>(min(chunk_rows, rows - r) * nK);
+    const uint32_t bar = smem_u32(&full[i % kStages]);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load_g2s(smem_u32(stage + (i % kStages) * kStageBytes), band + (long long)r * nK, bytes, bar);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbarrier_init();
+    for (int i = 0; i < min(kStages, n_chunks); ++i) issue(i);  // the first copies start at once
+    cta_total = 0;
+    abort_flag = 0;
+  }
+  for (int r = tid; r < rows_per_cta; r += kThreads) row_acc[r] = 0;
+  __syncthreads();
+  // first cluster barrier phase: arrive now, wait before the first access to another
+  // rank's shared memory (by then every CTA of the cluster has started)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  const int cpr = nK / 16;
+  const int c = tid % cpr, r_off = tid / cpr, r_step = kThreads / cpr;
+  const bool active = r_off < r_step;
+  const bool warp_row = (cpr % 32) == 0;  // a warp's 32 units lie in one row
+  // nK a power of two: every thread is active and a full stage gives each exactly
+  // kStageUnits units (rows r_off + k * r_step); a row's cpr units are one lane group
+  // (cpr < 32) or whole warps (cpr >= 32)
+  const bool pow2 = (kThreads % cpr) == 0;
+  int cols[16];
+#pragma unroll
+  for (int b = 0; b < 16; ++b) cols[b] = 0;
+  uint32_t acc[4] = {0, 0, 0, 0};  // byte-wide column counters, flushed before they can pass 255
+  int pending = 0;
+  auto flush_cols = [&]() {
+#pragma unroll
+    for (int b = 0; b < 16; ++b) cols[b] += (acc[b >> 2] >> (8 * (b & 3))) & 0xff;
+    acc[0] = acc[1] = acc[2] = acc[3] = 0;
+    pending = 0;
+  };
+  int failed = -1;  // first chunk whose wait gave up
+  for (int i = 0; i < n_chunks; ++i) {
+    const bool ok = __all_sync(0xffffffffu, wait_stage(smem_u32(&full[i % kStages]), (i / kStages) & 1,
+                                                       &abort_flag, err));
+    const unsigned char* src = stage + (i % kStages) * kStageBytes + c * 16;
+    const int base = i * chunk_rows;
+    const int nr = min(chunk_rows, rows - base);
+    if (ok && pow2 && nr == chunk_rows) {
+      uint4 x[kStageUnits];
+      uint32_t any = 0;
+#pragma unroll
+      for (int k = 0; k < kStageUnits; ++k) {
+        x[k] = *reinterpret_cast<const uint4*>(src + (r_off + k * r_step) * nK);
+        any |= x[k].x | x[k].y | x[k].z | x[k].w;
+      }
+      if (!__all_sync(0xffffffffu, (any & 0xfefefefeu) == 0)) {
+        // some byte of the warp's units is neither 0 nor 1: reduce every byte to a 0/1 flag
+#pragma unroll
+        for (int k = 0; k < kStageUnits; ++k) {
+          x[k].x = nonzero_byte_flags(x[k].x); x[k].y = nonzero_byte_flags(x[k].y);
+          x[k].z = nonzero_byte_flags(x[k].z); x[k].w = nonzero_byte_flags(x[k].w);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kStageUnits; ++k) {
+        acc[0] += x[k].x; acc[1] += x[k].y; acc[2] += x[k].z; acc[3] += x[k].w;
+        // byte-wise sum of the four flag words (each byte <= 4), then the sum of its bytes
+        int cnt = __dp4a(x[k].x + x[k].y + x[k].z + x[k].w, 0x01010101u, 0u);
+        const int row = base + r_off + k * r_step;
+        if (warp_row) {
+          cnt = __reduce_add_sync(0xffffffffu, cnt);
+          if ((tid & 31) == 0 && cnt) atomicAdd(&row_acc[row], cnt);
+        } else {
+          for (int off = 1; off < cpr; off <<= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+          if (c == 0) row_acc[row] = cnt;  // the lane group holds the whole row
+        }
+      }
+      pending += kStageUnits;
+      if (pending + kStageUnits > 255) flush_cols();
+    } else if (ok && active) {
+      for (int rl = r_off; rl < nr; rl += r_step) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src + rl * nK);
+        const uint32_t f0 = nonzero_byte_flags(x.x), f1 = nonzero_byte_flags(x.y);
+        const uint32_t f2 = nonzero_byte_flags(x.z), f3 = nonzero_byte_flags(x.w);
+        acc[0] += f0; acc[1] += f1; acc[2] += f2; acc[3] += f3;
+        int cnt = __popc(f0) + __popc(f1) + __popc(f2) + __popc(f3);
+        if (warp_row) {
+          cnt = __reduce_add_sync(0xffffffffu, cnt);
+          if ((tid & 31) == 0 && cnt) atomicAdd(&row_acc[base + rl], cnt);
+        } else if (cnt) {
+          atomicAdd(&row_acc[base + rl], cnt);
+        }
+        if (++pending == 255) flush_cols();
+      }
+    }
+    if (!__syncthreads_and(ok)) {  // every thread has read stage i % kStages, or the CTA gives up
+      failed = i;
+      break;
+    }
+    if (tid == 0 && i + kStages < n_chunks) issue(i + kStages);
+  }
+  if (failed >= 0) {
+    if (tid == 0) {
+      // let the copies still in flight land before the ring is reused or the CTA exits
+      for (int j = failed; j < min(failed + kStages, n_chunks); ++j) {
+        const uint32_t bar = smem_u32(&full[j % kStages]);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar, (j / kStages) & 1) && globaltimer() - t0 < kDrainLimitNs) {
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // row loads (exact per CTA) and the CTA's total
+  int local = 0;
+  for (int r = tid; r < rows; r += kThreads) {
+    const int v = row_acc[r];
+    row_loads[head * nQ + row0 + r] = v;
+    local += v;
+  }
+  local = __reduce_add_sync(0xffffffffu, local);
+  if ((tid & 31) == 0 && local) atomicAdd(&cta_total, local);
+
+  // column partials: each thread's 16 counts go to its own slot of the (now idle) stage
+  // ring, [r_off][nK] ints (r_step * nK * 4 <= 16 KB); a thread then sums 4 adjacent
+  // columns over the r_step slots and pushes the sums (one 16-byte store) into the
+  // shared memory of the rank that owns them (column j belongs to rank j / slice, slice
+  // a multiple of 4), at row `rank` of that rank's [n_ranks][slice] receive buffer.
+  // Pushing (remote stores) instead of pulling (remote loads) leaves one cluster barrier
+  // and no remote round trips.
+  int* slot = reinterpret_cast<int*>(stage);
+  if (active) {
+#pragma unroll
+    for (int b = 0; b < 16; b += 4) {
+      int4 v;
+      v.x = cols[b + 0] + ((acc[b >> 2] >> 0) & 0xff);
+      v.y = cols[b + 1] + ((acc[b >> 2] >> 8) & 0xff);
+      v.z = cols[b + 2] + ((acc[b >> 2] >> 16) & 0xff);
+      v.w = cols[b + 3] + ((acc[b >> 2] >> 24) & 0xff);
+      *reinterpret_cast<int4*>(slot + r_off * nK + c * 16 + b) = v;
+    }
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid == 0) cluster.map_shared_rank(head_part, 0)[rank] = cta_total;
+  const int slice = ((nK + n_ranks - 1) / n_ranks + 3) & ~3;
+  for (int j = 4 * tid; j < nK; j += 4 * kThreads) {
+    int4 sum = make_int4(0, 0, 0, 0);
+    for (int q = 0; q < r_step; ++q) {
+      const int4 v = *reinterpret_cast<const int4*>(slot + q * nK + j);
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    const int owner = j / slice;
+    *reinterpret_cast<int4*>(cluster.map_shared_rank(recv, owner) + rank * slice + (j - owner * slice)) = sum;
+  }
+  cluster.sync();  // every rank's pushes have landed
+
+  const int j0 = rank * slice, j1 = min(nK, j0 + slice);
+  for (int j = j0 + tid; j < j1; j += kThreads) {
+    int sum = 0;
+    for (int q = 0; q < n_ranks; ++q) sum += recv[q * slice + (j - j0)];
+    col_loads[head * nK + j] = sum;
+  }
+  if (rank == 0 && tid == 0 && head_loads) {
+    int sum = 0;
+    for (int q = 0; q < n_ranks; ++q) sum += head_part[q];
+    head_loads[head] = sum;
+  }
+}
+
 // KV-block loads summed over (b, h): thread j adds column j of every head.
 __global__ void __launch_bounds__(kThreads) kv_block_loads_kernel(const int32_t* __restrict__ col_loads,
                                                                   int groups, int nK,
@@ -186,7 +429,7 @@ extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, 
   if (B < 1 || H < 1 || nQ < 1 || nK < 1) return DBSP_ERR_INVALID_ARG;
   const long long total = (long long)B * H * nQ * nK;
   if (total >= (1LL << 31) || (long long)B * H > 65535) return DBSP_ERR_INVALID_ARG;
-  if (nK > kMaxCols) return DBSP_ERR_UNSUPPORTED;
+  if (nK > kMaxCols || nQ > kMaxRows) return DBSP_ERR_UNSUPPORTED;
   if (!dbsp::aligned(row_loads, 4) || !dbsp::aligned(col_loads, 4) ||
       (head_loads && !dbsp::aligned(head_loads, 4)))
     return DBSP_ERR_INVALID_ARG;
@@ -200,12 +443,10 @@ extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, 
   ranks = std::min(ranks, nQ);
   const int rows_per_cta = (nQ + ranks - 1) / ranks;
   ranks = (nQ + rows_per_cta - 1) / rows_per_cta;
-  const size_t smem = sizeof(int) * ((size_t)nK + rows_per_cta);
-
   const bool vec = (nK % 16 == 0) && dbsp::aligned(mask, 16);
-  auto kernel = vec ? mask_loads_kernel<16> : mask_loads_kernel<1>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads)");
+  const size_t part_bytes = sizeof(int) * ((size_t)nK + 4 * kMaxCluster + rows_per_cta);
+  const bool stream_rows = vec && nK <= kStreamMaxCols && part_bytes + kStages * kStageBytes <= kStreamMaxSmem;
+  const size_t smem = part_bytes + (stream_rows ? (size_t)kStages * kStageBytes : 0);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ranks, B * H, 1);
@@ -219,6 +460,27 @@ extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaError_t e;
+  if (stream_rows) {
+    e = cudaFuncSetAttribute(mask_loads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads)");
+    if (kMaxCluster > 8) {
+      e = cudaFuncSetAttribute(mask_loads_stream_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads cluster)");
+    }
+    const int chunk_rows = kStageBytes / nK;
+    e = cudaLaunchKernelEx(&cfg, mask_loads_stream_kernel, mask, nQ, nK, rows_per_cta, chunk_rows, row_loads,
+                           col_loads, head_loads, dbsp::error_word(dev));
+    if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch mask_loads");
+    return DBSP_OK;
+  }
+  auto kernel = vec ? mask_loads_kernel<16> : mask_loads_kernel<1>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads)");
+  if (kMaxCluster > 8) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads cluster)");
+  }
   e = cudaLaunchKernelEx(&cfg, kernel, mask, nQ, nK, rows_per_cta, row_loads, col_loads, head_loads);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch mask_loads");
   return DBSP_OK;

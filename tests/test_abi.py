@@ -56,6 +56,7 @@ FAKE = 1 << 20  # never dereferenced: validation fails first
     ((FAKE, 0, 1, 1, 1, FAKE, FAKE, None, None), 1),            # B = 0
     ((FAKE, 1, 1, 1, 1, None, FAKE, None, None), 1),            # null row loads
     ((FAKE, 1, 1, 8, 20000, FAKE, FAKE, None, None), 2),        # nK beyond the kernel
+    ((FAKE, 1, 1, 131073, 8, FAKE, FAKE, None, None), 2),       # nQ beyond the kernel
     ((FAKE, 1, 1, 1, 1, FAKE + 2, FAKE, None, None), 1),        # misaligned int32 output
     ((FAKE, 70000, 1, 1, 1, FAKE, FAKE, None, None), 1),        # B*H beyond the grid
 ])

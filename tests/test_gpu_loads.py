@@ -35,7 +35,12 @@ def test_workload_masks(built_library, cuda_device, name):
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (2, 3, 5, 7), (1, 2, 16, 48), (1, 1, 300, 16),
-                                   (2, 2, 1000, 33), (1, 1, 4, 16384), (3, 1, 2048, 64), (1, 5, 9, 8)])
+                                   (2, 2, 1000, 33), (1, 1, 4, 16384), (3, 1, 2048, 64), (1, 5, 9, 8),
+                                   # rows streamed through shared memory: a ragged last stage, 96 units
+                                   # per row (a quarter of the threads idle), 256 units per row, and
+                                   # bands long enough that per-thread byte counters are flushed
+                                   (1, 2, 37, 4096), (1, 1, 70, 1536), (1, 1, 8192, 1024),
+                                   (1, 1, 2048, 4096), (1, 1, 131072, 16), (1, 1, 3, 4112)])
 @pytest.mark.parametrize("density", [0.0, 0.3, 1.0])
 def test_random_masks(built_library, cuda_device, shape, density):
     rng = np.random.default_rng(hash((shape, density)) % 2**32)
