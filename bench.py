@@ -80,6 +80,8 @@ def workload_description(w):
 def bench_config(w, n_workers, n_dense, world=1):
     """The ``config`` object of the JSON line; both arms print the same one."""
     return {"workload": workload_description(w), "n_workers": n_workers, "worklist": "LPT",
+            "plan_cost": "dense blocks per item (block_cost 1, item_cost 0); shard passes add "
+                         "an item cost of 4 blocks, fitted from cta_timing",
             "dense_blocks": n_dense, "items": w.n_items,
             "l2": "flushed by a 256 MiB write before every timed GPU step (outside the events)",
             "parallelism": "replicas" if world > 1 else "single GPU"}
@@ -441,6 +443,9 @@ def run_gpu(args):
 
 
 # ----------------------------------------------------------------------------- suite (all workloads)
+L2_BYTES = 129 * 1000 * 1000  # GB300 L2
+
+
 def _time_ms(fn, stream, flush, reps):
     import torch
 
@@ -505,11 +510,34 @@ def run_suite(args):
         nbytes = mask_np.size + 4 * (w.B * w.H * (w.nQ + w.nK + 1))
         line["mask_loads"] = {"us": 1e3 * t, "GB/s": nbytes / t / 1e6, "bytes": nbytes,
                               "frac_of_hbm": nbytes / t / 1e6 / float(peaks["hbm_gbs"])}
+        # back to back: R launches captured in one CUDA graph (no host in the loop), cycling
+        # through enough copies of the mask (together more than twice the 129 MB L2) that
+        # each launch reads its mask from HBM; per-launch time without the event overhead
+        copies = int(min(16, max(2, -(-2 * L2_BYTES // mask_np.size))))
+        masks = [mask.clone() for _ in range(copies)]
+        R = 4 * copies
+        side = torch.cuda.Stream(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            dbsp.dbsp_block_mask_loads(masks[0], pb.row_loads, pb.col_loads, pb.head_loads, stream=side)
+            side.synchronize()
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(R):
+                    dbsp.dbsp_block_mask_loads(masks[i % copies], pb.row_loads, pb.col_loads, pb.head_loads,
+                                               stream=side)
+        tb = _time_ms(graph.replay, stream, flush, 5) / R
+        line["mask_loads"]["back_to_back"] = {
+            "us": 1e3 * tb, "GB/s": nbytes / tb / 1e6, "frac_of_hbm": nbytes / tb / 1e6 / float(peaks["hbm_gbs"]),
+            "launches": R, "mask_copies": copies, "from_hbm": bool(copies * mask_np.size > 2 * L2_BYTES),
+            "how": "CUDA graph of the launches"}
+        del graph
+        del masks
         # a2: LPT plan
         plan = lambda: dbsp.dbsp_plan_lpt(pb.row_loads.view(-1), m, pb.worker_of, pb.worker_offsets, pb.worklist,
                                           pb.worker_loads, stream=stream)
         line["lpt_plan"] = {"us": 1e3 * _time_ms(plan, stream, flush, reps)}
         # a3/a4: attention under three worklists
+        obs = []  # per CTA: (units, dense blocks, busy us), over all three worklists
         for kind in ("lpt", "round_robin", "contiguous"):
             if kind == "lpt":
                 off, wl = pb.worker_offsets, pb.worklist
@@ -524,11 +552,32 @@ def run_suite(args):
                                    "frac_of_bf16_peak": flop / t / 1e9 / float(peaks["bf16_tflops"]),
                                    "sm_skew": float((busy.max() - busy.mean()) / busy.mean()),
                                    "blocks_max_over_mean": float(tt[:, 2].max() / max(1e-9, tt[:, 2].mean()))}
-            if kind == "lpt":  # busy ~ a * items + b * blocks per CTA (least squares)
-                units = np.diff(off.cpu().numpy()).astype(np.float64)
-                coef = np.linalg.lstsq(np.stack([units, tt[:, 2].astype(np.float64)], 1), busy / 1e3,
-                                       rcond=None)[0]
-                line["attn_lpt"]["fit"] = {"us_per_item": float(coef[0]), "us_per_block": float(coef[1])}
+            units = np.diff(off.cpu().numpy()).astype(np.float64)
+            obs.append(np.stack([units, tt[:, 2].astype(np.float64), busy / 1e3], 1))
+        # f3: planning cost fitted from cta_timing. busy ~ a * items + b * blocks per CTA, by
+        # least squares over the CTAs of all three worklists (under LPT alone items and
+        # blocks per CTA move together and the fit is ill-conditioned); then the A/B of an
+        # LPT plan on block_cost * row_load + item_cost with item_cost / block_cost = a / b
+        X = np.concatenate(obs)
+        coef = np.linalg.lstsq(X[:, :2], X[:, 2], rcond=None)[0]
+        c0 = float(coef[0] / coef[1]) if coef[1] > 0 else 0.0
+        bc, ic = P.PLAN_BLOCK_COST_SCALE, int(round(max(0.0, c0) * P.PLAN_BLOCK_COST_SCALE))
+        line["cost_fit"] = {"us_per_item": float(coef[0]), "us_per_block": float(coef[1]), "item_in_blocks": c0,
+                            "ctas": int(X.shape[0])}
+        # A/B: LPT on block_cost * row_load + item_cost at a few item costs (in blocks),
+        # the fitted one included; the first entry is the pages' plan on dense blocks
+        line["cost_ab"] = {}
+        costs = [(1, 0), (1, 2), (1, P.ITEM_COST_BLOCKS), (1, 8), (bc, ic)]
+        for bc2, ic2 in dict.fromkeys(costs):
+            pc = P.plan(mask, m, block_cost=bc2, item_cost=ic2)
+            fn = lambda: dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, pc.worker_offsets,
+                                                         pc.worklist, m, out=out, lse=lse, cta_timing=timing,
+                                                         stream=stream)
+            t = _time_ms(fn, stream, flush, max(7, reps))
+            tt = timing.view(m, 3).cpu().numpy()
+            busy = (tt[:, 1] - tt[:, 0]).astype(np.float64)
+            line["cost_ab"][f"{bc2}:{ic2}"] = {"us": 1e3 * t, "TFLOP/s": flop / t / 1e9,
+                                              "sm_skew": float((busy.max() - busy.mean()) / busy.mean())}
         # head-level LPT over a few "virtual GPUs" (db-SP blog, scenario 1): makespan
         # against the lower bound max(ceil(total / m), largest head)
         hl = pb.head_loads.view(-1).contiguous()
@@ -581,6 +630,12 @@ def run_suite(args):
                                            "shard_max_over_mean": float(shard_load.max() / shard_load.mean())}
                 if t_sp is not None:
                     line[f"merge_{layout}"]["shard_plan_us"] = 1e3 * t_sp
+                # A/B of the shard passes' planning cost (block_cost:item_cost)
+                ab = {}
+                for bc2, ic2 in dict.fromkeys([(1, 0), (8, 1), (P.SHARD_BLOCK_COST, P.SHARD_ITEM_COST)]):
+                    plans = [P.plan(shards[s], m, block_cost=bc2, item_cost=ic2) for s in range(n_sh)]
+                    ab[f"{bc2}:{ic2}"] = {"partials_us": 1e3 * _time_ms(partials, stream, flush, max(5, reps))}
+                line[f"merge_{layout}"]["cost_ab"] = ab
         line["peaks"] = {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
         status = dbsp.dbsp_device_status()
         line["device_status"] = status

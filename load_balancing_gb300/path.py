@@ -114,10 +114,18 @@ def attention_partial(q, k, v, mask, block, causal, p, o_part, m_part, l_part, s
                                     scale=scale, stream=stream)
 
 
-# Planning loads of a shard's partial pass: a dense block counts 8, an item 1 (an item
-# without dense blocks costs its output rows, about an eighth of a block's MMA time).
-SHARD_BLOCK_COST = 8
-SHARD_ITEM_COST = 1
+# Planning cost of one item, in dense blocks. Besides its dense blocks an item costs its
+# Q tile, its mask-row scan and its epilogue. A least-squares fit of per-CTA busy time
+# (cta_timing) to items and blocks per CTA, over the CTAs of three worklists on the
+# LLM-heads workload, gives 2.88 us per item and 0.683 us per block: 4.2 blocks per item.
+ITEM_COST_BLOCKS = 4
+PLAN_BLOCK_COST_SCALE = 8  # block cost at which a measured item/block ratio is rounded
+# A shard's partial pass leaves many items with few or no dense blocks; planned on dense
+# blocks alone, every empty item lands on the same (least-loaded) worker. Shard passes
+# therefore plan on row_load + ITEM_COST_BLOCKS. Whole-mask plans keep the pages' dense-
+# block loads: there the item cost gained nothing measurable.
+SHARD_BLOCK_COST = 1
+SHARD_ITEM_COST = ITEM_COST_BLOCKS
 
 
 def sharded_attention(q, k, v, shard_masks, block, causal, n_workers, scale=0.0, stream=None):
