@@ -84,6 +84,7 @@ def bench_config(w, n_workers, n_dense, world=1):
                          "an item cost of 4 blocks, fitted from cta_timing",
             "dense_blocks": n_dense, "items": w.n_items,
             "l2": "flushed by a 256 MiB write before every timed GPU step (outside the events)",
+            "step": "one CUDA graph of the mask-loads, LPT-plan and attention launches, replayed per step",
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
@@ -319,20 +320,24 @@ def run_gpu(args):
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
-    def step(e=None):
+    def step(e=None, st=None):
+        st = stream if st is None else st
         if e:
-            e[0].record(stream)
+            e[0].record(st)
         dbsp.dbsp_block_mask_loads(mask, plan_buf.row_loads, plan_buf.col_loads, plan_buf.head_loads,
-                                   stream=stream)
+                                   stream=st)
         dbsp.dbsp_plan_lpt(plan_buf.row_loads.view(-1), n_workers, plan_buf.worker_of, plan_buf.worker_offsets,
-                           plan_buf.worklist, plan_buf.worker_loads, stream=stream)
+                           plan_buf.worklist, plan_buf.worker_loads, stream=st)
         if e:
-            e[1].record(stream)
+            e[1].record(st)
         dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, plan_buf.worker_offsets,
                                         plan_buf.worklist, n_workers, out=out, lse=lse, cta_timing=timing,
-                                        stream=stream)
+                                        stream=st)
         if e:
-            e[2].record(stream)
+            e[2].record(st)
+
+    def step_on(st):
+        step(None, st)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -341,6 +346,25 @@ def run_gpu(args):
     status = dbsp.dbsp_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
+    # the timed step is one CUDA graph of the three launches (no host work between them;
+    # each kernel may start its prologue while the previous one finishes)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graph_lp = torch.cuda.CUDAGraph()  # mask loads + plan alone (breakdown)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step_on(side)
+        with torch.cuda.graph(graph_lp, stream=side):
+            dbsp.dbsp_block_mask_loads(mask, plan_buf.row_loads, plan_buf.col_loads, plan_buf.head_loads,
+                                       stream=side)
+            dbsp.dbsp_plan_lpt(plan_buf.row_loads.view(-1), n_workers, plan_buf.worker_of,
+                               plan_buf.worker_offsets, plan_buf.worklist, plan_buf.worker_loads, stream=side)
+    stream.wait_stream(side)
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
     if rank == 0:
@@ -348,17 +372,31 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    skews = []
     for i in range(args.steps):
         flush.zero_()  # L2 flush, outside the timed events
-        step(ev[i])
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    plan_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    # breakdown (not part of the value): the same kernels launched from the host, with an
+    # event between the plan and the attention kernel
+    for i in range(args.steps):
+        flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize(dev)
     attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    plan_ms = []
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        graph_lp.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    plan_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     total_s = sum(step_ms) / 1e3
     total_s = max_over_ranks(total_s, world, dev)
     t = timing.view(n_workers, 3).cpu().numpy()

@@ -769,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
+  griddep_wait();  // worklist, mask and Q/K/V may come from the previous grid
 
   if (warp < kSoftmaxWarp0) {
     setmaxnreg_dec<kRegsControl>();
@@ -786,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
     setmaxnreg_inc<kRegsSoftmax>();
     run_softmax<BLOCK, D, UNITS>(p, c, tmem, smem_u32(base), &to);
   }
+  griddep_launch_dependents();  // this CTA's work is done; the next grid may start its prologue
 
   tc_fence_before();
   __syncthreads();
@@ -837,8 +839,8 @@ int launch_attn_t(const void* q, const void* k, const void* v, const AttnParams&
   auto kernel = attn_fwd_kernel<BLOCK, D, UNITS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(attn)");
-  kernel<<<n_workers, kThreads, smem, stream>>>(tq, tk, tv, to, p);
-  DBSP_LAUNCH_CHECK("launch attn_fwd");
+  e = dbsp::launch_overlapped(kernel, dim3(n_workers), dim3(kThreads), smem, stream, tq, tk, tv, to, p);
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch attn_fwd");
   return DBSP_OK;
 }
 

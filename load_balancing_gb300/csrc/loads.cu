@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
   int* col_part = smem;               // [nK]
   int* row_acc = smem + nK;           // [rows_per_cta]
   __shared__ int cta_total;
+  griddep_wait();  // the mask may come from the previous grid
+  griddep_launch_dependents();
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -214,6 +216,8 @@ __global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
   __shared__ int cta_total;
   __shared__ int head_part[kMaxCluster];  // rank 0: every rank's total
   __shared__ volatile int abort_flag;
+  griddep_wait();  // the mask may come from the previous grid
+  griddep_launch_dependents();
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -453,13 +457,14 @@ extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, 
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ranks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = dbsp::overlap_previous_grid();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e;
   if (stream_rows) {
     e = cudaFuncSetAttribute(mask_loads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -28,6 +29,8 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(
     const float* __restrict__ o_parts, const float* __restrict__ m_parts,
     const float* __restrict__ l_parts, int n_shards, long long rows, int d,
     __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  dbsp::ptx::griddep_wait();  // the partials come from the previous grids
+  dbsp::ptx::griddep_launch_dependents();
   const int quads = d >> 2;
   const int groups = (quads + kQuads - 1) / kQuads;  // threads per row
   const long long total = rows * groups;
@@ -110,6 +113,8 @@ __global__ void __launch_bounds__(kThreads) merge_pieces_kernel(
     const int32_t* __restrict__ split_item, const int32_t* __restrict__ split_off,
     const int32_t* __restrict__ counts, int max_slots, int n_items, int nQ, int S, int block, int d,
     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int* err) {
+  dbsp::ptx::griddep_wait();  // the pieces come from the previous grid
+  dbsp::ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int n_split = counts[2];
   const int n_slots = min(counts[3], max_slots);  // slots that hold pieces, within the buffers
@@ -183,9 +188,10 @@ extern "C" int dbsp_merge_partials(const float* o_parts, const float* m_parts, c
   const long long units = rows * ((d / 4 + kQuads - 1) / kQuads);
   const long long want = (units + kThreads - 1) / kThreads;
   const int blocks = (int)std::min<long long>(want, (long long)dbsp::sm_count(dev) * 8);
-  merge_partials_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      o_parts, m_parts, l_parts, n_shards, rows, d, static_cast<__nv_bfloat16*>(out), lse);
-  DBSP_LAUNCH_CHECK("launch merge_partials");
+  const cudaError_t e = dbsp::launch_overlapped(merge_partials_kernel, dim3(blocks), dim3(kThreads), 0,
+                                                static_cast<cudaStream_t>(stream), o_parts, m_parts, l_parts,
+                                                n_shards, rows, d, static_cast<__nv_bfloat16*>(out), lse);
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch merge_partials");
   return DBSP_OK;
 }
 
@@ -206,9 +212,10 @@ extern "C" int dbsp_merge_pieces(const float* o_piece, const float* m_piece, con
   if (st != DBSP_OK) return st;
   const long long want = (n_items * block + (kThreads / 32) - 1) / (kThreads / 32);
   const int blocks = (int)std::max<long long>(1, std::min<long long>(want, (long long)dbsp::sm_count(dev) * 8));
-  merge_pieces_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      o_piece, m_piece, l_piece, split_item, split_off, counts, max_slots, (int)n_items, S / block, S, block, d,
+  const cudaError_t e = dbsp::launch_overlapped(
+      merge_pieces_kernel, dim3(blocks), dim3(kThreads), 0, static_cast<cudaStream_t>(stream), o_piece, m_piece,
+      l_piece, split_item, split_off, counts, max_slots, (int)n_items, S / block, S, block, d,
       static_cast<__nv_bfloat16*>(out), lse, dbsp::error_word(dev));
-  DBSP_LAUNCH_CHECK("launch merge_pieces");
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch merge_pieces");
   return DBSP_OK;
 }

@@ -38,6 +38,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -549,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     const int32_t* __restrict__ loads, const int32_t* __restrict__ home, int n_max, const int32_t* n_dev, int m,
     int bonus, int bc, int ic, int32_t* __restrict__ worker_of, int32_t* __restrict__ offsets,
     int32_t* __restrict__ worklist, int64_t* __restrict__ worker_loads, int* err) {
+  dbsp::ptx::griddep_wait();  // the loads come from the previous grid
+  dbsp::ptx::griddep_launch_dependents();
   // the item count: n_max, or the first *n_dev items when the count lives on the device
   const int n = n_dev ? min(n_max, max(0, *n_dev)) : n_max;
   extern __shared__ __align__(16) unsigned char dyn[];
@@ -840,9 +843,17 @@ int launch(const int32_t* loads, const int32_t* home, int n, const int32_t* n_de
   auto kernel = lpt_plan_kernel<KMAX>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(lpt_plan)");
-  kernel<<<1, kThreads, kDynBytes, s>>>(loads, home, n, n_dev, m, bonus, bc, ic, worker_of, offsets, worklist,
-                                        worker_loads, err);
-  DBSP_LAUNCH_CHECK("launch lpt_plan");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kDynBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {dbsp::overlap_previous_grid()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, loads, home, n, n_dev, m, bonus, bc, ic, worker_of, offsets, worklist,
+                         worker_loads, err);
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch lpt_plan");
   return DBSP_OK;
 }
 

@@ -69,6 +69,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch. A grid launched with programmatic stream serialization
+// may start while the grid before it in the stream is still running; griddep_wait
+// blocks until that grid has completed and its memory operations are visible (it
+// returns at once when there is no such grid), so it must precede every read of the
+// previous grid's results and every write the previous grid might still read.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid in the stream launch before this one has finished; that grid's own
+// griddep_wait still waits for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- registers
 // Per-warpgroup register budget change; every warp of the warpgroup executes it.
 template <uint32_t N>
