@@ -337,6 +337,9 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
     const int run_end = bin_end[bin];
     const int ws = (max_load - bin) * bc + ic;       // planning load of item s
     const unsigned long long key0 = A[0];
+    // every stored load after this batch lies in [L0, L0 + span): the largest is at most
+    // the current largest plus ws (the items are in descending order of load)
+    const int span = (int)min((long long)R, (long long)(A[m - 1] >> kWorkerBits) - L0 + ws + 1);
     const int p0 = (int)(key0 & kWorkerMask);
     if (ws == 0) {  // zero loads never change a key: the rest goes to the minimum
       const int c0 = counts[p0];
@@ -427,10 +430,10 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
       s += bp;
     }
     __syncthreads();  // the buckets are final for this batch
-    // ---- counting sort: exclusive scan of the bucket counts from L0 over the ring
+    // ---- counting sort: exclusive scan of the bucket counts from L0 over the span
     {
-      const int per = (R + kThreads - 1) / kThreads;
-      const int i0 = min(R, tid * per), i1 = min(R, i0 + per);
+      const int per = (span + kThreads - 1) / kThreads;
+      const int i0 = min(span, tid * per), i1 = min(span, i0 + per);
       int tot = 0;
       for (int i = i0; i < i1; ++i) tot += bcnt[(L0 + i) & rmask];
       int incl = tot;
@@ -451,13 +454,13 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
       }
     }
     __syncthreads();
-    int bad = 0;  // a load outside [L0, L0 + R) or a position outside [0, m): inconsistent state
+    int bad = 0;  // a load outside [L0, L0 + span) or a position outside [0, m): inconsistent state
 #pragma unroll
     for (int k = 0; k < kWorkersPerThread; ++k) {
       const int p = tid + k * kThreads;
       if (p < m) {
         const int L = Lw[p];
-        if ((unsigned)(L - L0) >= (unsigned)R) {
+        if ((unsigned)(L - L0) >= (unsigned)span) {
           bad = 1;
           continue;
         }
