@@ -79,6 +79,19 @@ DBSP_API int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, in
                           void* stream);
 
 /*
+ * Mask loads of causal attention.  [6D attention notes §2.3]: under a causal mask the
+ * KV blocks after a Q block's diagonal are skipped, so only the dense blocks on or below
+ * the diagonal (column <= row) are work. As dbsp_block_mask_loads, counting only those:
+ * the loads of a mask that was not clipped to the diagonal beforehand, which is what
+ * dbsp_plan_lpt should balance for dbsp_block_sparse_attn_fwd with causal = 1.
+ * Requires nQ == nK (otherwise DBSP_ERR_INVALID_ARG); every other argument and limit as
+ * in dbsp_block_mask_loads.
+ */
+DBSP_API int dbsp_block_mask_loads_causal(const uint8_t* mask, int B, int H, int nQ, int nK,
+                                          int32_t* row_loads, int32_t* col_loads, int32_t* head_loads,
+                                          void* stream);
+
+/*
  * KV-block loads across heads.  [db-SP blog, scenario 2]: a KV-block's load is the
  * number of dense blocks in its mask column; when the KV sequence is split into
  * shards shared by every head (sequence parallelism), the load that a shard

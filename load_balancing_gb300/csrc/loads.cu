@@ -57,9 +57,26 @@ __device__ __forceinline__ uint32_t nonzero_byte_flags(uint32_t x) {
   return ((((x & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x) >> 7) & 0x01010101u;
 }
 
+// Causal variant: only the blocks on or below the diagonal (column <= row) count. Keeps
+// the bytes of the 16 columns [col0, col0 + 16) of row `row` that satisfy it.
+__device__ __forceinline__ uint4 keep_causal(uint4 x, int col0, int row) {
+  const int keep = row - col0 + 1;  // columns of the unit at or before the diagonal
+  if (keep >= 16) return x;
+  if (keep <= 0) return make_uint4(0u, 0u, 0u, 0u);
+  auto word_mask = [&](int k) -> uint32_t {
+    const int nb = keep - 4 * k;  // bytes kept of word k
+    return nb >= 4 ? 0xffffffffu : (nb <= 0 ? 0u : (1u << (8 * nb)) - 1u);
+  };
+  x.x &= word_mask(0);
+  x.y &= word_mask(1);
+  x.z &= word_mask(2);
+  x.w &= word_mask(3);
+  return x;
+}
+
 // VEC = 16: each work unit is 16 consecutive mask bytes of one row (uint4 loads);
-// VEC = 1: one byte.
-template <int VEC>
+// VEC = 1: one byte. CAUSAL: count only the blocks on or below the diagonal.
+template <int VEC, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
     const uint8_t* __restrict__ mask, int nQ, int nK, int rows_per_cta,
     int32_t* __restrict__ row_loads, int32_t* __restrict__ col_loads,
@@ -115,6 +132,7 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
             const int ru = r + u * r_step;
             x[u] = ru < row1 ? __ldg(reinterpret_cast<const uint4*>(head_mask + (long long)ru * nK) + c)
                              : make_uint4(0u, 0u, 0u, 0u);
+            if (CAUSAL) x[u] = keep_causal(x[u], c * 16, ru);
           }
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u) {
@@ -146,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) mask_loads_kernel(
       } else {
         int col = 0;
         for (int r = row0 + r_off; r < row1; r += r_step) {
-          const int nz = __ldg(head_mask + (long long)r * nK + c) != 0;
+          const int nz = (!CAUSAL || c <= r) && __ldg(head_mask + (long long)r * nK + c) != 0;
           col += nz;
           if (nz) atomicAdd(&row_acc[r - row0], 1);
         }
@@ -204,6 +222,7 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity, volati
 // (chunk_rows * nK <= kStageBytes). Thread t owns the 16-byte column unit t % (nK / 16)
 // and, within a stage, every (256 / (nK / 16))-th row from t / (nK / 16); its per-byte
 // column counters therefore stay in registers across the whole band.
+template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
     const uint8_t* __restrict__ mask, int nQ, int nK, int rows_per_cta, int chunk_rows,
     int32_t* __restrict__ row_loads, int32_t* __restrict__ col_loads, int32_t* __restrict__ head_loads,
@@ -281,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
 #pragma unroll
       for (int k = 0; k < kStageUnits; ++k) {
         x[k] = *reinterpret_cast<const uint4*>(src + (r_off + k * r_step) * nK);
+        if (CAUSAL) x[k] = keep_causal(x[k], c * 16, row0 + base + r_off + k * r_step);
         any |= x[k].x | x[k].y | x[k].z | x[k].w;
       }
       if (!__all_sync(0xffffffffu, (any & 0xfefefefeu) == 0)) {
@@ -309,7 +329,8 @@ __global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
       if (pending + kStageUnits > 255) flush_cols();
     } else if (ok && active) {
       for (int rl = r_off; rl < nr; rl += r_step) {
-        const uint4 x = *reinterpret_cast<const uint4*>(src + rl * nK);
+        uint4 x = *reinterpret_cast<const uint4*>(src + rl * nK);
+        if (CAUSAL) x = keep_causal(x, c * 16, row0 + base + rl);
         const uint32_t f0 = nonzero_byte_flags(x.x), f1 = nonzero_byte_flags(x.y);
         const uint32_t f2 = nonzero_byte_flags(x.z), f3 = nonzero_byte_flags(x.w);
         acc[0] += f0; acc[1] += f1; acc[2] += f2; acc[3] += f3;
@@ -426,10 +447,13 @@ extern "C" int dbsp_kv_block_loads(const int32_t* col_loads, int groups, int nK,
   return DBSP_OK;
 }
 
-extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK,
-                                     int32_t* row_loads, int32_t* col_loads,
-                                     int32_t* head_loads, void* stream) {
+namespace {
+
+template <bool CAUSAL>
+int mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK, int32_t* row_loads, int32_t* col_loads,
+               int32_t* head_loads, void* stream) {
   if (!mask || !row_loads || !col_loads) return DBSP_ERR_INVALID_ARG;
+  if (CAUSAL && nQ != nK) return DBSP_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || nQ < 1 || nK < 1) return DBSP_ERR_INVALID_ARG;
   const long long total = (long long)B * H * nQ * nK;
   if (total >= (1LL << 31) || (long long)B * H > 65535) return DBSP_ERR_INVALID_ARG;
@@ -467,19 +491,20 @@ extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, 
   cfg.numAttrs = 2;
   cudaError_t e;
   if (stream_rows) {
-    e = cudaFuncSetAttribute(mask_loads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(mask_loads_stream_kernel<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads)");
     if (kMaxCluster > 8) {
-      e = cudaFuncSetAttribute(mask_loads_stream_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(mask_loads_stream_kernel<CAUSAL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads cluster)");
     }
     const int chunk_rows = kStageBytes / nK;
-    e = cudaLaunchKernelEx(&cfg, mask_loads_stream_kernel, mask, nQ, nK, rows_per_cta, chunk_rows, row_loads,
+    e = cudaLaunchKernelEx(&cfg, mask_loads_stream_kernel<CAUSAL>, mask, nQ, nK, rows_per_cta, chunk_rows, row_loads,
                            col_loads, head_loads, dbsp::error_word(dev));
     if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch mask_loads");
     return DBSP_OK;
   }
-  auto kernel = vec ? mask_loads_kernel<16> : mask_loads_kernel<1>;
+  auto kernel = vec ? mask_loads_kernel<16, CAUSAL> : mask_loads_kernel<1, CAUSAL>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "cudaFuncSetAttribute(mask_loads)");
   if (kMaxCluster > 8) {
@@ -489,4 +514,17 @@ extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, 
   e = cudaLaunchKernelEx(&cfg, kernel, mask, nQ, nK, rows_per_cta, row_loads, col_loads, head_loads);
   if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch mask_loads");
   return DBSP_OK;
+}
+
+}  // namespace
+
+extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK, int32_t* row_loads,
+                                     int32_t* col_loads, int32_t* head_loads, void* stream) {
+  return mask_loads<false>(mask, B, H, nQ, nK, row_loads, col_loads, head_loads, stream);
+}
+
+extern "C" int dbsp_block_mask_loads_causal(const uint8_t* mask, int B, int H, int nQ, int nK,
+                                            int32_t* row_loads, int32_t* col_loads, int32_t* head_loads,
+                                            void* stream) {
+  return mask_loads<true>(mask, B, H, nQ, nK, row_loads, col_loads, head_loads, stream);
 }

@@ -30,6 +30,7 @@ _SIGNATURES = {
     "dbsp_status_string": (ctypes.c_char_p, [_i32]),
     "dbsp_last_error_string": (ctypes.c_char_p, []),
     "dbsp_block_mask_loads": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "dbsp_block_mask_loads_causal": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "dbsp_kv_block_loads": (_i32, [_vp, _i32, _i32, _vp, _vp]),
     "dbsp_plan_lpt": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "dbsp_plan_lpt_cost": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp,
@@ -121,6 +122,16 @@ def dbsp_block_mask_loads(mask, row_loads, col_loads, head_loads=None, stream=No
         _ptr(col_loads, torch.int32, "col_loads"), _ptr(head_loads, torch.int32, "head_loads", True),
         _stream(stream))
     _check(st, "dbsp_block_mask_loads")
+
+
+def dbsp_block_mask_loads_causal(mask, row_loads, col_loads, head_loads=None, stream=None):
+    """As dbsp_block_mask_loads, counting only the blocks on or below the diagonal (nQ == nK)."""
+    B, H, nQ, nK = mask.shape
+    st = library().dbsp_block_mask_loads_causal(
+        _ptr(mask, torch.uint8, "mask"), B, H, nQ, nK, _ptr(row_loads, torch.int32, "row_loads"),
+        _ptr(col_loads, torch.int32, "col_loads"), _ptr(head_loads, torch.int32, "head_loads", True),
+        _stream(stream))
+    _check(st, "dbsp_block_mask_loads_causal")
 
 
 def dbsp_kv_block_loads(col_loads, kv_loads, stream=None):

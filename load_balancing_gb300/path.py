@@ -36,15 +36,24 @@ def alloc_plan(B, H, nQ, nK, n_workers, device):
                 torch.empty(n_workers, dtype=torch.int64, device=device), n_workers)
 
 
-def plan(mask, n_workers, home=None, stay_bonus=0, out=None, stream=None, block_cost=1, item_cost=0):
+def _mask_loads(mask, row_loads, col_loads, head_loads, causal, stream):
+    # causal: count only the blocks on or below the diagonal, the ones causal attention
+    # computes (a mask need not be clipped to the diagonal beforehand)
+    fn = dbsp.dbsp_block_mask_loads_causal if causal else dbsp.dbsp_block_mask_loads
+    fn(mask, row_loads, col_loads, head_loads, stream=stream)
+
+
+def plan(mask, n_workers, home=None, stay_bonus=0, out=None, stream=None, block_cost=1, item_cost=0, causal=False):
     """Loads of ``mask`` [B,H,nQ,nK] (uint8, CUDA) and the LPT worklist over (b,h,qb) items.
 
     The default plans on dense-block counts, as the pages do; ``block_cost`` and
-    ``item_cost`` plan on ``row_load * block_cost + item_cost`` instead.
+    ``item_cost`` plan on ``row_load * block_cost + item_cost`` instead. With ``causal``
+    the loads count only the blocks on or below the diagonal (pass it for causal
+    attention unless the mask is already clipped to the diagonal).
     """
     B, H, nQ, nK = mask.shape
     p = out or alloc_plan(B, H, nQ, nK, n_workers, mask.device)
-    dbsp.dbsp_block_mask_loads(mask, p.row_loads, p.col_loads, p.head_loads, stream=stream)
+    _mask_loads(mask, p.row_loads, p.col_loads, p.head_loads, causal, stream)
     if block_cost == 1 and item_cost == 0:
         dbsp.dbsp_plan_lpt(p.row_loads.view(-1), n_workers, p.worker_of, p.worker_offsets, p.worklist,
                            p.worker_loads, home=home, stay_bonus=stay_bonus, stream=stream)
@@ -138,7 +147,8 @@ def sharded_attention(q, k, v, shard_masks, block, causal, n_workers, scale=0.0,
     l_parts = torch.empty((n_sh, B, H, S), dtype=torch.float32, device=dev)
     for s in range(n_sh):
         # a shard leaves many items without dense blocks: an item cost spreads them
-        ps = plan(shard_masks[s], n_workers, stream=stream, block_cost=SHARD_BLOCK_COST, item_cost=SHARD_ITEM_COST)
+        ps = plan(shard_masks[s], n_workers, stream=stream, block_cost=SHARD_BLOCK_COST, item_cost=SHARD_ITEM_COST,
+                  causal=bool(causal))
         attention_partial(q, k, v, shard_masks[s], block, causal, ps, o_parts[s], m_parts[s], l_parts[s],
                           scale=scale, stream=stream)
     out = torch.empty_like(q)
@@ -189,7 +199,7 @@ def alloc_split_plan(B, H, nQ, nK, n_workers, block, d, max_pieces, max_slots, d
 
 
 def plan_split(mask, n_workers, block, d, max_piece_load=0, max_pieces=4, max_slots=None, block_cost=1,
-               item_cost=0, out=None, stream=None):
+               item_cost=0, out=None, stream=None, causal=False):
     """Mask loads -> split plan -> LPT over the units, all on the device (no host sync).
 
     ``max_piece_load`` T <= 0 selects half the mean load per worker. With that choice a
@@ -198,13 +208,14 @@ def plan_split(mask, n_workers, block, d, max_piece_load=0, max_pieces=4, max_sl
     With a fixed T the default is the worst case n_items * max_pieces; the piece buffers
     take max_slots * block * (d + 2) * 4 bytes, so pass a smaller ``max_slots`` for large
     problems (a plan that needs more pieces reports DBSP_ERR_UNSUPPORTED on the device).
+    ``causal`` counts only the blocks on or below the diagonal, as in ``plan``.
     """
     B, H, nQ, nK = mask.shape
     n = B * H * nQ
     if max_slots is None:
         max_slots = n * max_pieces if max_piece_load > 0 else min(n * max_pieces, 4 * n_workers)
     sp = out or alloc_split_plan(B, H, nQ, nK, n_workers, block, d, max_pieces, max_slots, mask.device)
-    dbsp.dbsp_block_mask_loads(mask, sp.row_loads, sp.col_loads, sp.head_loads, stream=stream)
+    _mask_loads(mask, sp.row_loads, sp.col_loads, sp.head_loads, causal, stream)
     dbsp.dbsp_split_plan(sp.row_loads.view(-1), n_workers, max_piece_load, max_pieces, sp.max_slots, sp.unit_item,
                          sp.unit_pk, sp.unit_slot, sp.unit_load, sp.split_item, sp.split_off, sp.counts,
                          stream=stream)

@@ -64,6 +64,14 @@ def test_mask_loads_host_validation(built_library, args, expect):
     from load_balancing_gb300 import dbsp
 
     assert dbsp.library().dbsp_block_mask_loads(*args) == expect
+    # the causal variant checks the same, and first that the mask is square
+    assert dbsp.library().dbsp_block_mask_loads_causal(*args) == (expect if args[3] == args[4] else 1)
+
+
+def test_causal_mask_loads_need_a_square_mask(built_library):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_block_mask_loads_causal(FAKE, 1, 1, 8, 16, FAKE, FAKE, None, None) == 1
 
 
 @pytest.mark.parametrize("args,expect", [

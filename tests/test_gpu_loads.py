@@ -83,3 +83,30 @@ def test_kv_block_loads(built_library, cuda_device, name):
     dbsp.dbsp_kv_block_loads(col, kv)
     assert dbsp.dbsp_device_status() == 0
     np.testing.assert_array_equal(kv.cpu().numpy(), OL.kv_block_loads(mask_np))
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 16, 16), (2, 3, 64, 64), (1, 1, 1024, 1024), (1, 2, 300, 300),
+                                   (1, 1, 4112, 4112), (1, 1, 33, 33)])
+def test_causal_loads_count_only_blocks_on_or_below_the_diagonal(built_library, cuda_device, shape):
+    """dbsp_block_mask_loads_causal on masks that are NOT clipped to the diagonal equals
+    the oracle's loads of the same masks clipped to it (6D notes §2.3: the blocks after
+    a Q block's diagonal are skipped): streamed rows (16 and 64 KV blocks, 1024 with the
+    unrolled path), byte rows (300, 33) and 16-byte register rows (4112)."""
+    from load_balancing_gb300 import dbsp
+
+    rng = np.random.default_rng(sum(shape))
+    vals = rng.integers(1, 256, shape).astype(np.uint8)
+    mask_np = np.where(rng.random(shape) < 0.5, vals, 0).astype(np.uint8)
+    dev = torch.device("cuda:0")
+    B, H, nQ, nK = shape
+    mask = torch.from_numpy(mask_np).to(dev)
+    row = torch.full((B, H, nQ), -7, dtype=torch.int32, device=dev)
+    col = torch.full((B, H, nK), -7, dtype=torch.int32, device=dev)
+    head = torch.full((B, H), -7, dtype=torch.int32, device=dev)
+    dbsp.dbsp_block_mask_loads_causal(mask, row, col, head)
+    assert dbsp.dbsp_device_status() == 0
+    clipped = np.where(np.tril(np.ones((nQ, nK), dtype=bool)), mask_np, 0).astype(np.uint8)
+    r, c, h = OL.block_mask_loads(clipped)
+    np.testing.assert_array_equal(row.cpu().numpy(), r)
+    np.testing.assert_array_equal(col.cpu().numpy(), c)
+    np.testing.assert_array_equal(head.cpu().numpy(), h)

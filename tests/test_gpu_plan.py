@@ -205,3 +205,24 @@ def test_bucket_ring_limits(built_library, cuda_device, m, wmaxes):
             loads[rng.random(n) < 0.2] = max(0, wmax // 3)  # a long run of equal loads
             loads[0] = wmax
             _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+
+
+def test_causal_plan_of_an_unclipped_mask(built_library, cuda_device):
+    """path.plan(causal=True) on a causal mask that still holds blocks above the diagonal
+    plans exactly what the oracle's LPT gives for the loads of the mask clipped to the
+    diagonal (the blocks causal attention computes); without the flag the plan differs."""
+    from load_balancing_gb300 import path as P
+
+    rng = np.random.default_rng(21)
+    shape = (1, 4, 48, 48)
+    mask_np = (rng.random(shape) < 0.5).astype(np.uint8)
+    mask = torch.from_numpy(mask_np).to("cuda:0")
+    clipped = np.where(np.tril(np.ones(shape[2:], dtype=bool)), mask_np, 0).astype(np.uint8)
+    row, _, _ = OL.block_mask_loads(clipped)
+    ref = OP.lpt_plan(row.reshape(-1), 9)
+    p = P.plan(mask, 9, causal=True)
+    got = {"worker_of": p.worker_of.cpu().numpy(), "offsets": p.worker_offsets.cpu().numpy(),
+           "worklist": p.worklist.cpu().numpy(), "worker_loads": p.worker_loads.cpu().numpy()}
+    _assert_same(got, ref)
+    q = P.plan(mask, 9)
+    assert not np.array_equal(q.worker_loads.cpu().numpy(), got["worker_loads"])
