@@ -483,23 +483,31 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
   return true;
 }
 
-// Phase 2 with a bonus: one item at a time (one warp).
-template <int KMAX>
+// Phase 2 with a bonus: one item at a time (one warp). K is int when every key fits 31
+// bits (then one warp minimum per item), else long long (two, over the halves).
+template <int KMAX, typename K>
 __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t* __restrict__ loads,
                               const int32_t* __restrict__ home, int bonus, int bc, int ic, int n, int m, int cm,
                               int* counts,
                               long long* final_load, int32_t* __restrict__ worker_of) {
+  constexpr K kNone = sizeof(K) == 4 ? (K)INT_MAX : (K)kKeyNone;
   const int lane = threadIdx.x & 31;
-  long long key[KMAX];
+  K key[KMAX];
   int cnt[KMAX];
 #pragma unroll
   for (int q = 0; q < KMAX; ++q) {
     const int p = lane + 32 * q;
-    key[q] = p < m ? (long long)p : kKeyNone;  // load 0, worker p
+    key[q] = p < m ? (K)p : kNone;  // load 0, worker p
     cnt[q] = 0;
   }
-  long long my_min = lane_minimum(key);
-  const long long bonus_key = (long long)bonus << kWorkerBits;
+  auto lane_min = [&]() {
+    K v = key[0];
+#pragma unroll
+    for (int q = 1; q < KMAX; ++q) v = key[q] < v ? key[q] : v;
+    return v;
+  };
+  K my_min = lane_min();
+  const K bonus_key = (K)bonus << kWorkerBits;
   for (int base = 0; base < n; base += 32) {
     const int t = base + lane;
     int my_i = 0, my_w = 0, my_h = -1;
@@ -513,38 +521,41 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
       const int i = __shfl_sync(0xffffffffu, my_i, s);
       const int w = __shfl_sync(0xffffffffu, my_w, s);
       const int h = __shfl_sync(0xffffffffu, my_h, s);
-      long long cand = my_min;
-      if (h >= 0 && (h & 31) == lane) {
-        long long kh = kKeyNone;
+      // the lane holding the home worker offers its key lowered by the bonus (branch-free:
+      // every lane evaluates it, so the warp never diverges on the way to the minimum)
+      K kh = kNone;
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) kh = q == (h >> 5) ? key[q] : kh;
-        kh -= bonus_key;
-        cand = kh < cand ? kh : cand;
+      for (int q = 0; q < KMAX; ++q) kh = q == (h >> 5) ? key[q] : kh;
+      kh -= bonus_key;
+      const K cand = (h >= 0 && (h & 31) == lane && kh < my_min) ? kh : my_min;
+      int p;
+      if constexpr (sizeof(K) == 4) {
+        p = __reduce_min_sync(0xffffffffu, (int)cand) & (int)kWorkerMask;
+      } else {
+        const int hi = (int)(cand >> 32);
+        const int min_hi = __reduce_min_sync(0xffffffffu, hi);
+        const unsigned lo = hi == min_hi ? (unsigned)(cand & 0xffffffffu) : 0xffffffffu;
+        const unsigned min_lo = __reduce_min_sync(0xffffffffu, lo);
+        p = (int)(min_lo & (unsigned)kWorkerMask);
       }
-      const int hi = (int)(cand >> 32);
-      const int min_hi = __reduce_min_sync(0xffffffffu, hi);
-      const unsigned lo = hi == min_hi ? (unsigned)(cand & 0xffffffffu) : 0xffffffffu;
-      const unsigned min_lo = __reduce_min_sync(0xffffffffu, lo);
-      const int p = (int)(min_lo & (unsigned)kWorkerMask);
-      if ((p & 31) == lane) {
-        const int qp = p >> 5;
-        int rank = 0;
+      const bool mine = (p & 31) == lane;  // the lane holding the chosen worker
+      const int qp = mine ? p >> 5 : -1;
+      int rank = 0;
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) {
-          const bool me = q == qp;
-          rank = me ? cnt[q] : rank;
-          cnt[q] += me;
-          key[q] += me ? ((long long)w << kWorkerBits) : 0;
-        }
-        worker_of[i] = p + cm * rank;
-        my_min = lane_minimum(key);
+      for (int q = 0; q < KMAX; ++q) {
+        const bool me = q == qp;
+        rank = me ? cnt[q] : rank;
+        cnt[q] += me;
+        key[q] += me ? ((K)w << kWorkerBits) : (K)0;
       }
+      if (mine) worker_of[i] = p + cm * rank;
+      my_min = lane_min();
     }
   }
 #pragma unroll
   for (int q = 0; q < KMAX; ++q) {
     const int p = lane + 32 * q;
-    if (p < m) { counts[p] = cnt[q]; final_load[p] = key[q] >> kWorkerBits; }
+    if (p < m) { counts[p] = cnt[q]; final_load[p] = (long long)(key[q] >> kWorkerBits); }
   }
 }
 
@@ -786,7 +797,14 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
       greedy_batched<KT, long long>(sorted, bin_end, nbins, max_load, n, m, cm, bc, ic, keys[0], counts, final_load,
                                     worker_of, sh.scan);
   } else if (tid < 32) {
-    greedy_serial<KMAX>(sorted, loads, home, bonus, bc, ic, n, m, cm, counts, final_load, worker_of);
+    // a worker takes an item only while its key, lowered by at most the bonus, is the
+    // smallest: every load stays below total / m + the largest planning load + bonus
+    const bool key32 =
+        sh.total_load / (unsigned long long)m + (unsigned long long)max_load * bc + ic + (unsigned)bonus < (1ull << 19);
+    if (key32)
+      greedy_serial<KMAX, int>(sorted, loads, home, bonus, bc, ic, n, m, cm, counts, final_load, worker_of);
+    else
+      greedy_serial<KMAX, long long>(sorted, loads, home, bonus, bc, ic, n, m, cm, counts, final_load, worker_of);
   }
   __syncthreads();
 
