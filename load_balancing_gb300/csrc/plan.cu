@@ -333,7 +333,12 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
   };
   while (s < n) {
     if (++batches > max_batches) return false;
-    while (bin < nbins && bin_end[bin] <= s) ++bin;  // the run that holds item s
+    // the run that holds item s: read off its staged load, else walk the bins
+    if (sload) {
+      bin = max_load - (int)sload[s];
+    } else {
+      while (bin < nbins && bin_end[bin] <= s) ++bin;
+    }
     const int run_end = bin_end[bin];
     const int ws = (max_load - bin) * bc + ic;       // planning load of item s
     const unsigned long long key0 = A[0];
