@@ -822,6 +822,12 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     for (int p = tid; p < m; p += kThreads) worker_loads[p] = final_load[p];
   const bool wvec = (reinterpret_cast<uintptr_t>(worker_of) & 15u) == 0;
   const int nw4 = wvec ? n / 4 : 0;
+  // The worklist is a scatter (item i to offsets[p] + rank). With the greedy done, the
+  // dynamic shared memory is free: for large plans that fit, the worklist is assembled
+  // there and written out with coalesced stores instead of one scattered global store
+  // per item (imbalance workload, 40,960 items: 180 -> 166 us).
+  int* ws = n >= 8192 && (size_t)n * sizeof(int) <= kDynBytes ? reinterpret_cast<int*>(dyn) : nullptr;
+  int32_t* wdst = ws ? ws : worklist;
   for (int base = tid; base < nw4; base += kU * kThreads) {
     int4 c4[kU];
 #pragma unroll
@@ -838,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
         for (int e = 0; e < 4; ++e) {
           const int p = cm == DBSP_MAX_WORKERS ? (cc[e] & (DBSP_MAX_WORKERS - 1)) : cc[e] % m;
           const int rank = cm == DBSP_MAX_WORKERS ? (cc[e] >> 10) : cc[e] / m;
-          worklist[counts[p] + rank] = 4 * i4 + e;
+          wdst[counts[p] + rank] = 4 * i4 + e;
           pp[e] = p;
         }
         reinterpret_cast<int4*>(worker_of)[i4] = make_int4(pp[0], pp[1], pp[2], pp[3]);
@@ -855,10 +861,17 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
       if (i < n) {
         const int p = cm == DBSP_MAX_WORKERS ? (code[u] & (DBSP_MAX_WORKERS - 1)) : code[u] % m;
         const int rank = cm == DBSP_MAX_WORKERS ? (code[u] >> 10) : code[u] / m;
-        worklist[counts[p] + rank] = i;
+        wdst[counts[p] + rank] = i;
         worker_of[i] = p;
       }
     }
+  }
+  if (ws) {
+    __syncthreads();
+    const bool lvec = (reinterpret_cast<uintptr_t>(worklist) & 15u) == 0;
+    const int nl4 = lvec ? n / 4 : 0;
+    for (int q = tid; q < nl4; q += kThreads) reinterpret_cast<int4*>(worklist)[q] = reinterpret_cast<const int4*>(ws)[q];
+    for (int q = 4 * nl4 + tid; q < n; q += kThreads) worklist[q] = ws[q];
   }
 }
 

@@ -226,3 +226,13 @@ def test_causal_plan_of_an_unclipped_mask(built_library, cuda_device):
     _assert_same(got, ref)
     q = P.plan(mask, 9)
     assert not np.array_equal(q.worker_loads.cpu().numpy(), got["worker_loads"])
+
+
+@pytest.mark.parametrize("n,hi,m", [(8191, 60, 152), (8192, 60, 152), (46000, 30, 152), (46085, 30, 152)])
+def test_worklist_assembled_in_shared_memory(built_library, cuda_device, n, hi, m):
+    """From 8,192 items up to what fits the kernel's dynamic shared memory (46,084
+    int32), the worklist is assembled in shared memory and copied out; either side of
+    both limits the plan is the oracle's."""
+    rng = np.random.default_rng(n)
+    loads = rng.integers(0, hi, n)
+    _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
