@@ -108,6 +108,23 @@ DBSP_API int dbsp_kv_block_loads(const int32_t* col_loads, int groups, int nK, i
                                  void* stream);
 
 /*
+ * The block masks of KV shards.  [db-SP blog, scenario 2]: when the KV sequence is
+ * split into shards, each shard's pass attends only to the KV blocks it holds. Given
+ * the shard of every KV block (e.g. worker_of of dbsp_plan_lpt over dbsp_kv_block_loads),
+ * out[s] is mask with every column j of another shard (shard_of[j] != s) cleared.
+ *
+ *   mask      uint8 [B, H, nQ, nK]
+ *   shard_of  int32 [nK], values in [0, n_shards); a value outside that range sets
+ *             DBSP_ERR_INVALID_ARG on the device and clears column j in every shard.
+ *   out       uint8 [n_shards, B, H, nQ, nK]  out; must not overlap mask.
+ * Requires B, H, nQ, nK, n_shards >= 1, n_shards <= 65535 and B*H*nQ*nK < 2^31. The
+ * mask is read once; one kernel launch (16-byte accesses when nK % 16 == 0 and both
+ * byte pointers are 16-byte aligned, byte by byte otherwise).
+ */
+DBSP_API int dbsp_shard_masks(const uint8_t* mask, int B, int H, int nQ, int nK, const int32_t* shard_of,
+                              int n_shards, uint8_t* out, void* stream);
+
+/*
  * LPT plan with stay-in-place bonus.  [db-SP blog, scenario 1]: repeatedly give
  * the largest remaining item to the currently least-loaded worker (LPT).
  * [db-SP blog, scenario 2, third bullet]: an item placed on its original worker

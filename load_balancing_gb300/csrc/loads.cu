@@ -431,6 +431,47 @@ __global__ void __launch_bounds__(kThreads) kv_block_loads_kernel(const int32_t*
   kv_loads[j] = s;
 }
 
+// KV-shard masks: thread u takes 16 mask bytes (VEC = 16) or one (VEC = 1) and writes
+// them to every shard with the columns of the other shards cleared.
+template <int VEC>
+__global__ void __launch_bounds__(kThreads) shard_masks_kernel(const uint8_t* __restrict__ mask, long long units,
+                                                               int nK, const int32_t* __restrict__ shard_of,
+                                                               int n_shards, uint8_t* __restrict__ out, int* err) {
+  griddep_wait();  // the mask and the shard plan may come from the previous grids
+  griddep_launch_dependents();
+  const long long total = units * VEC;  // mask bytes
+  const long long stride = (long long)gridDim.x * kThreads;
+  for (long long u = (long long)blockIdx.x * kThreads + threadIdx.x; u < units; u += stride) {
+    const int col0 = (int)((u * VEC) % nK);
+    if constexpr (VEC == 16) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(mask) + u);
+      int sh[16];
+#pragma unroll
+      for (int b = 0; b < 16; ++b) {
+        sh[b] = __ldg(shard_of + col0 + b);
+        if ((unsigned)sh[b] >= (unsigned)n_shards) dbsp::report(err, DBSP_ERR_INVALID_ARG);
+      }
+      for (int s = 0; s < n_shards; ++s) {
+        uint32_t keep[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t k = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) k |= (sh[4 * w + b] == s ? 0xffu : 0u) << (8 * b);
+          keep[w] = k;
+        }
+        const uint4 y = make_uint4(x.x & keep[0], x.y & keep[1], x.z & keep[2], x.w & keep[3]);
+        reinterpret_cast<uint4*>(out + (long long)s * total)[u] = y;
+      }
+    } else {
+      const uint8_t x = __ldg(mask + u);
+      const int sh = __ldg(shard_of + col0);
+      if ((unsigned)sh >= (unsigned)n_shards) dbsp::report(err, DBSP_ERR_INVALID_ARG);
+      for (int s = 0; s < n_shards; ++s) out[(long long)s * total + u] = sh == s ? x : (uint8_t)0;
+    }
+  }
+}
+
 }  // namespace
 
 extern "C" int dbsp_kv_block_loads(const int32_t* col_loads, int groups, int nK, int32_t* kv_loads,
@@ -527,4 +568,28 @@ extern "C" int dbsp_block_mask_loads_causal(const uint8_t* mask, int B, int H, i
                                             int32_t* row_loads, int32_t* col_loads, int32_t* head_loads,
                                             void* stream) {
   return mask_loads<true>(mask, B, H, nQ, nK, row_loads, col_loads, head_loads, stream);
+}
+
+extern "C" int dbsp_shard_masks(const uint8_t* mask, int B, int H, int nQ, int nK, const int32_t* shard_of,
+                                int n_shards, uint8_t* out, void* stream) {
+  if (!mask || !shard_of || !out) return DBSP_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || nQ < 1 || nK < 1 || n_shards < 1 || n_shards > 65535) return DBSP_ERR_INVALID_ARG;
+  const long long total = (long long)B * H * nQ * nK;
+  if (total >= (1LL << 31)) return DBSP_ERR_INVALID_ARG;
+  if (!dbsp::aligned(shard_of, 4)) return DBSP_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = dbsp::check_device(&dev);
+  if (st != DBSP_OK) return st;
+  const bool vec = nK % 16 == 0 && dbsp::aligned(mask, 16) && dbsp::aligned(out, 16);
+  const long long units = vec ? total / 16 : total;
+  const int blocks = (int)std::max<long long>(
+      1, std::min<long long>((units + kThreads - 1) / kThreads, (long long)dbsp::sm_count(dev) * 8));
+  cudaError_t e = vec ? dbsp::launch_overlapped(shard_masks_kernel<16>, dim3(blocks), dim3(kThreads), 0,
+                                                static_cast<cudaStream_t>(stream), mask, units, nK, shard_of,
+                                                n_shards, out, dbsp::error_word(dev))
+                      : dbsp::launch_overlapped(shard_masks_kernel<1>, dim3(blocks), dim3(kThreads), 0,
+                                                static_cast<cudaStream_t>(stream), mask, units, nK, shard_of,
+                                                n_shards, out, dbsp::error_word(dev));
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch shard_masks");
+  return DBSP_OK;
 }

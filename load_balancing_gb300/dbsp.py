@@ -31,6 +31,7 @@ _SIGNATURES = {
     "dbsp_last_error_string": (ctypes.c_char_p, []),
     "dbsp_block_mask_loads": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "dbsp_block_mask_loads_causal": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "dbsp_shard_masks": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
     "dbsp_kv_block_loads": (_i32, [_vp, _i32, _i32, _vp, _vp]),
     "dbsp_plan_lpt": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "dbsp_plan_lpt_cost": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp,
@@ -132,6 +133,18 @@ def dbsp_block_mask_loads_causal(mask, row_loads, col_loads, head_loads=None, st
         _ptr(col_loads, torch.int32, "col_loads"), _ptr(head_loads, torch.int32, "head_loads", True),
         _stream(stream))
     _check(st, "dbsp_block_mask_loads_causal")
+
+
+def dbsp_shard_masks(mask, shard_of, n_shards, out=None, stream=None):
+    """mask uint8 [B,H,nQ,nK], shard_of int32 [nK] -> uint8 [n_shards,B,H,nQ,nK]: each shard's KV blocks only."""
+    B, H, nQ, nK = mask.shape
+    if out is None:
+        out = torch.empty((n_shards, B, H, nQ, nK), dtype=torch.uint8, device=mask.device)
+    st = library().dbsp_shard_masks(_ptr(mask, torch.uint8, "mask"), B, H, nQ, nK,
+                                    _ptr(shard_of, torch.int32, "shard_of"), int(n_shards),
+                                    _ptr(out, torch.uint8, "out"), _stream(stream))
+    _check(st, "dbsp_shard_masks")
+    return out
 
 
 def dbsp_kv_block_loads(col_loads, kv_loads, stream=None):

@@ -96,10 +96,9 @@ def plan_kv_shards(mask, n_shards, stream=None):
     return sp
 
 
-def shard_masks_from_plan(mask, sp):
-    """uint8 [n_shards, B, H, nQ, nK]: ``mask`` restricted to each shard's KV blocks."""
-    owned = sp.shard_of.view(1, -1) == torch.arange(sp.n_shards, device=mask.device, dtype=torch.int32).view(-1, 1)
-    return mask.unsqueeze(0) * owned.to(torch.uint8).view(sp.n_shards, 1, 1, 1, -1)
+def shard_masks_from_plan(mask, sp, stream=None):
+    """uint8 [n_shards, B, H, nQ, nK]: ``mask`` restricted to each shard's KV blocks (one kernel)."""
+    return dbsp.dbsp_shard_masks(mask, sp.shard_of, sp.n_shards, stream=stream)
 
 
 def attention(q, k, v, mask, block, causal, p, out=None, lse=None, scale=0.0, cta_timing=None,

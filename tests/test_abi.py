@@ -192,3 +192,17 @@ def test_units_and_pieces_host_validation(built_library):
     assert lib.dbsp_merge_pieces(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 2, 512, 128, 128, FAKE, None,
                                  None) == 1  # negative slot capacity
     assert lib.dbsp_plan_lpt_cost_n(FAKE, None, 10, 4, 1, 0, FAKE, FAKE, FAKE, None, None) == 1
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, 1, 1, 4, 16, FAKE, 2, FAKE, None), 1),        # null mask
+    ((FAKE, 1, 1, 4, 16, None, 2, FAKE, None), 1),        # null shard_of
+    ((FAKE, 1, 1, 4, 16, FAKE, 0, FAKE, None), 1),        # no shards
+    ((FAKE, 1, 1, 4, 16, FAKE, 70000, FAKE, None), 1),    # too many shards
+    ((FAKE, 1, 1, 4, 16, FAKE + 2, 2, FAKE, None), 1),    # misaligned shard_of
+    ((FAKE, 70000, 70000, 4, 16, FAKE, 2, FAKE, None), 1),  # mask too large
+])
+def test_shard_masks_host_validation(built_library, args, expect):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_shard_masks(*args) == expect

@@ -110,3 +110,26 @@ def test_causal_loads_count_only_blocks_on_or_below_the_diagonal(built_library, 
     np.testing.assert_array_equal(row.cpu().numpy(), r)
     np.testing.assert_array_equal(col.cpu().numpy(), c)
     np.testing.assert_array_equal(head.cpu().numpy(), h)
+
+
+@pytest.mark.parametrize("shape,n_shards", [((1, 2, 16, 64), 8), ((2, 1, 7, 48), 3), ((1, 1, 5, 33), 4),
+                                            ((1, 3, 256, 256), 8)])
+def test_shard_masks(built_library, cuda_device, shape, n_shards):
+    """dbsp_shard_masks: shard s keeps exactly the columns j with shard_of[j] == s (16-byte
+    and byte paths); a shard index out of range clears its column and is reported."""
+    from load_balancing_gb300 import dbsp
+
+    rng = np.random.default_rng(sum(shape) + n_shards)
+    mask_np = rng.integers(0, 3, shape).astype(np.uint8)
+    shard_np = rng.integers(0, n_shards, shape[-1]).astype(np.int32)
+    dev = torch.device("cuda:0")
+    out = dbsp.dbsp_shard_masks(torch.from_numpy(mask_np).to(dev), torch.from_numpy(shard_np).to(dev), n_shards)
+    assert dbsp.dbsp_device_status() == 0
+    ref = np.stack([np.where(shard_np == s, mask_np, 0) for s in range(n_shards)]).astype(np.uint8)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+    bad = shard_np.copy()
+    bad[1] = n_shards  # outside [0, n_shards)
+    out = dbsp.dbsp_shard_masks(torch.from_numpy(mask_np).to(dev), torch.from_numpy(bad).to(dev), n_shards)
+    assert dbsp.dbsp_device_status() == dbsp.DBSP_ERR_INVALID_ARG
+    ref = np.stack([np.where(bad == s, mask_np, 0) for s in range(n_shards)]).astype(np.uint8)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
