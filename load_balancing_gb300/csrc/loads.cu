@@ -5,10 +5,12 @@
 // balances whole heads, whose load is the head's total.
 //
 // Design: a thread-block cluster of up to 8 CTAs per (b, h) head; each CTA counts a
-// band of rows. Row loads are exact per CTA and written directly; column partials
-// live in shared memory and are summed by cluster rank 0 through distributed shared
-// memory, so no global scratch or atomics on the outputs are needed and the outputs
-// need no prior zeroing. HBM-bound: every mask byte is read once.
+// band of rows. Row loads are exact per CTA and written directly; column partials are
+// combined through distributed shared memory (the streaming kernel pushes each rank's
+// sums into the rank that owns those columns; the others let rank 0 read every rank's
+// partials), so no global scratch or atomics on the outputs are needed and the outputs
+// need no prior zeroing. HBM-bound: every mask byte is read once. A causal
+// instantiation counts only the blocks on or below the diagonal.
 //
 // Rows of at most 4096 bytes on a 16-byte aligned mask (every block mask up to 4096
 // KV blocks) take the streaming kernel: one thread moves the band through a ring of
@@ -16,6 +18,9 @@
 // in flight without holding it in registers, and all 256 threads count from shared
 // memory. Longer rows use 16-byte register loads, and rows whose length or pointer
 // does not allow 16-byte access are read byte by byte.
+//
+// Also here: the KV-block loads summed over heads, and the block mask of each KV shard
+// (db-SP blog, scenario 2).
 #include <cooperative_groups.h>
 
 #include <algorithm>
