@@ -96,8 +96,9 @@ def build_wait_test():
     In that build every pipeline wait of the attention kernel gives up after 20 ms,
     and the V producer of CTA 0 leaves out its first tile (neither its arrival nor its
     copy is issued), so that a wait runs out and the abort / drain / TMEM-free teardown
-    runs. The product library never contains this code. Returns the path of the .so
-    (under _build/).
+    runs. Likewise the streaming mask-loads kernel: 20 ms stage waits, and CTA (0, 0)
+    leaves out its first stage. The product library never contains this code. Returns
+    the path of the .so (under _build/).
     """
     out_dir = os.path.dirname(WAIT_TEST_LIB)
     os.makedirs(out_dir, exist_ok=True)

@@ -54,7 +54,14 @@ static_assert(kStages * kStageBytes >= 16384, "the ring holds the column slots (
 constexpr int kStageUnits = kStageBytes / (16 * kThreads);  // 16-byte units per thread in a full stage
 static_assert(kStageUnits >= 1 && kStageUnits < 128, "stage size");
 constexpr size_t kStreamMaxSmem = 200 * 1024;       // streaming kernel: dynamic shared memory cap
+#ifdef DBSP_WAIT_TEST
+// Test build only (never the product library): stage waits give up after 20 ms, and
+// CTA (0, 0) of the streaming kernel leaves out its first stage (neither the arrival nor
+// the copy is issued), so that its wait runs out and the drain and cluster teardown run.
+constexpr uint64_t kWaitLimitNs = 20000000ull;       // 20 ms per stage wait
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s per stage wait
+#endif
 constexpr uint64_t kDrainLimitNs = 100000000ull;     // 100 ms per teardown wait
 
 // Number of non-zero bytes in a 32-bit word, as 0x01 flags per byte.
@@ -254,6 +261,9 @@ __global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
   const int tid = threadIdx.x;
 
   auto issue = [&](int i) {  // chunk i into stage i % kStages (thread 0 only)
+#ifdef DBSP_WAIT_TEST
+    if (i == 0 && blockIdx.x == 0 && blockIdx.y == 0) return;  // the left-out stage
+#endif
     const int r = i * chunk_rows;
     const uint32_t bytes = static_cast<uint32_t>(min(chunk_rows, rows - r) * nK);
     const uint32_t bar = smem_u32(&full[i % kStages]);

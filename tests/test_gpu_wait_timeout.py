@@ -10,6 +10,10 @@ in flight) runs in a child process next to the product library:
     set again), and the items of every other CTA still match the oracle;
   * the product library, on the same stream of the same process, then returns
     DBSP_OK and the whole output matches the oracle: the context stays usable.
+The streaming mask-loads kernel is tested the same way: in the test build its CTA
+(0, 0) leaves out the first of its shared-memory stages (arrival and copy), so its
+bounded stage wait runs out; the other heads' loads are still exact, and the product
+library then returns exact loads for every head.
 """
 
 import json
@@ -45,8 +49,10 @@ def _child(test_lib):
     product = dbsp.library()
     report = {}
 
+    p = P.plan(mask, m)  # planned by the product library: the test build's loads time out too
+    torch.cuda.synchronize()
+    assert dbsp.dbsp_device_status() == dbsp.DBSP_OK
     dbsp._lib = dbsp.open_library(test_lib)
-    p = P.plan(mask, m)
     off = p.worker_offsets.cpu().numpy()
     wl = p.worklist.cpu().numpy()
     statuses = []
@@ -88,3 +94,64 @@ def test_bounded_wait_runs_out(built_library, cuda_device):
     assert report["cta0_items"] > 0
     assert report["test_build_status"] == [dbsp.DBSP_ERR_TIMEOUT, dbsp.DBSP_ERR_TIMEOUT]
     assert report["product_status"] == dbsp.DBSP_OK
+
+
+def _loads_child(test_lib):
+    import numpy as np
+    import torch
+
+    from load_balancing_gb300 import dbsp
+    from oracle import loads as OL
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    # 4096 x 64 per head: 8 ranks of 512 rows each, two 16 KB stages per rank, so the
+    # second stage of CTA (0, 0) is still in flight when its first wait gives up
+    B, H, nQ, nK = 1, 2, 4096, 64
+    rng = np.random.default_rng(12)
+    mask_np = (rng.random((B, H, nQ, nK)) < 0.4).astype(np.uint8)
+    mask = torch.from_numpy(mask_np).to(dev)
+    r_ref, c_ref, h_ref = OL.block_mask_loads(mask_np)
+    product = dbsp.library()
+    report = {}
+
+    def run():
+        row = torch.full((B, H, nQ), -7, dtype=torch.int32, device=dev)
+        col = torch.full((B, H, nK), -7, dtype=torch.int32, device=dev)
+        head = torch.full((B, H), -7, dtype=torch.int32, device=dev)
+        dbsp.dbsp_block_mask_loads(mask, row, col, head)
+        return row.cpu().numpy(), col.cpu().numpy(), head.cpu().numpy(), dbsp.dbsp_device_status()
+
+    dbsp._lib = dbsp.open_library(test_lib)
+    row, col, head, st = run()
+    report["test_build_status"] = st
+    # CTA (0, 0) holds rows 0..511 of head 0; the other ranks' rows and head 1 are exact
+    report["other_rows_exact"] = bool((row[0, 0, 512:] == r_ref[0, 0, 512:]).all())
+    report["other_head_exact"] = bool((row[:, 1] == r_ref[:, 1]).all() and (col[:, 1] == c_ref[:, 1]).all()
+                                      and (head[:, 1] == h_ref[:, 1]).all())
+    dbsp._lib = product
+    row, col, head, st = run()
+    report["product_status"] = st
+    report["product_exact"] = bool((row == r_ref).all() and (col == c_ref).all() and (head == h_ref).all())
+    print("WAIT_TEST " + json.dumps(report))
+
+
+def test_bounded_stage_wait_of_mask_loads_runs_out(built_library, cuda_device):
+    from load_balancing_gb300 import build as lbuild
+
+    test_lib = lbuild.build_wait_test()
+    env = dict(os.environ)
+    env["PYTHONPATH"] = os.pathsep.join([HERE, os.path.dirname(HERE), env.get("PYTHONPATH", "")])
+    code = f"import test_gpu_wait_timeout as t; t._loads_child({test_lib!r})"
+    r = subprocess.run([sys.executable, "-c", code], cwd=HERE, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, f"child failed:\n{r.stdout}\n{r.stderr}"
+    line = [x for x in r.stdout.splitlines() if x.startswith("WAIT_TEST ")][-1]
+    report = json.loads(line[len("WAIT_TEST "):])
+    from load_balancing_gb300 import dbsp
+
+    assert report["test_build_status"] == dbsp.DBSP_ERR_TIMEOUT
+    assert report["other_rows_exact"]
+    assert report["other_head_exact"]
+    assert report["product_status"] == dbsp.DBSP_OK
+    assert report["product_exact"]
