@@ -40,7 +40,10 @@ def test_workload_masks(built_library, cuda_device, name):
                                    # per row (a quarter of the threads idle), 256 units per row, and
                                    # bands long enough that per-thread byte counters are flushed
                                    (1, 2, 37, 4096), (1, 1, 70, 1536), (1, 1, 8192, 1024),
-                                   (1, 1, 2048, 4096), (1, 1, 131072, 16), (1, 1, 3, 4112)])
+                                   (1, 1, 2048, 4096), (1, 1, 131072, 16), (1, 1, 3, 4112),
+                                   # 8 bands of 188 rows per head, 6 stages of 32 rows each, the
+                                   # last band shorter and ragged
+                                   (2, 2, 1500, 512)])
 @pytest.mark.parametrize("density", [0.0, 0.3, 1.0])
 def test_random_masks(built_library, cuda_device, shape, density):
     rng = np.random.default_rng(hash((shape, density)) % 2**32)
