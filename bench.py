@@ -84,8 +84,16 @@ def bench_config(w, n_workers, n_dense, world=1):
                          "an item cost of 4 blocks, fitted from cta_timing",
             "dense_blocks": n_dense, "items": w.n_items,
             "l2": "flushed by a 256 MiB write before every timed GPU step (outside the events)",
-            "step": "one CUDA graph of the mask-loads, LPT-plan and attention launches, replayed per step",
+            "step": "pipelined: batch i's attention runs on n_workers persistent CTAs (one per SM but one) "
+                    "while the mask loads and LPT plan of batch i+1 run on the remaining SM, into the "
+                    "second of two plan buffers; each timed step holds one attention and one loads + plan",
             "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def attention_workers(n_sm):
+    """Persistent attention CTAs of the timed step: one per SM but one, which runs the next
+    batch's mask loads and plan meanwhile."""
+    return max(1, n_sm - 1)
 
 
 def dense_blocks(mask_np, causal):
@@ -254,7 +262,7 @@ def run_reference(args):
     cores = len(os.sched_getaffinity(0))
     sample_heads = [0, 16]  # one global and one local head per step
     sub_mask = np.ascontiguousarray(mask_np[:, sample_heads])
-    m = args.workers  # the GPU arm's worker count: one per SM
+    m = args.workers  # the GPU arm's worker count: one per SM but one
 
     def step():
         t0 = time.perf_counter()
@@ -310,61 +318,41 @@ def run_gpu(args):
     flop_fa = flop - 0.5 * flop_per_block * n_diag  # diagonal blocks counted as half
     mask = torch.from_numpy(mask_np).to(dev)
     q, k, v = W.make_qkv(w, dev)
-    n_workers = P.default_workers(dev)
-    plan_buf = P.alloc_plan(w.B, w.H, w.nQ, w.nK, n_workers, dev)
+    n_sm = P.default_workers(dev)
+    n_workers = attention_workers(n_sm)
+    # the timed step: batch i's attention on n_workers SMs beside batch i+1's mask loads and
+    # plan on the remaining one (two plan buffers, kept by PipelinedSteps)
+    pipe = P.PipelinedSteps(w.B, w.H, w.nQ, w.nK, dev, n_workers=n_workers)
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
     timing = torch.zeros(3 * n_workers, dtype=torch.int64, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MiB > L2
-    stream = torch.cuda.current_stream(dev)
+    s_attn = torch.cuda.Stream(dev, priority=-1)
+    s_attn.wait_stream(torch.cuda.current_stream(dev))
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    def loads_plan(pb, m, st):
+        dbsp.dbsp_block_mask_loads(mask, pb.row_loads, pb.col_loads, pb.head_loads, stream=st)
+        dbsp.dbsp_plan_lpt(pb.row_loads.view(-1), m, pb.worker_of, pb.worker_offsets, pb.worklist,
+                           pb.worker_loads, stream=st)
 
-    def step(e=None, st=None):
-        st = stream if st is None else st
-        if e:
-            e[0].record(st)
-        dbsp.dbsp_block_mask_loads(mask, plan_buf.row_loads, plan_buf.col_loads, plan_buf.head_loads,
-                                   stream=st)
-        dbsp.dbsp_plan_lpt(plan_buf.row_loads.view(-1), n_workers, plan_buf.worker_of, plan_buf.worker_offsets,
-                           plan_buf.worklist, plan_buf.worker_loads, stream=st)
-        if e:
-            e[1].record(st)
-        dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, plan_buf.worker_offsets,
-                                        plan_buf.worklist, n_workers, out=out, lse=lse, cta_timing=timing,
-                                        stream=st)
-        if e:
-            e[2].record(st)
+    def attention(pb, m, st, cta_timing=None):
+        dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, w.block, w.causal, pb.worker_offsets, pb.worklist, m,
+                                        out=out, lse=lse, cta_timing=cta_timing, stream=st)
 
-    def step_on(st):
-        step(None, st)
+    def pipelined(n, ev=None):
+        for i in range(n):
+            with torch.cuda.stream(s_attn):
+                flush.zero_()  # L2 flush, outside the timed events
+            pipe.step(q, k, v, mask, w.block, w.causal, next_mask=mask, out=out, lse=lse, cta_timing=timing,
+                      stream=s_attn, events=ev[i] if ev else None)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
+    pipe.prime(mask, stream=s_attn)  # batch 0's plan
+    pipelined(args.warmup)
     torch.cuda.synchronize(dev)
     status = dbsp.dbsp_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
-    # the timed step is one CUDA graph of the three launches (no host work between them;
-    # each kernel may start its prologue while the previous one finishes)
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream(dev)
-    side.wait_stream(stream)
-    graph_lp = torch.cuda.CUDAGraph()  # mask loads + plan alone (breakdown)
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(graph, stream=side):
-            step_on(side)
-        with torch.cuda.graph(graph_lp, stream=side):
-            dbsp.dbsp_block_mask_loads(mask, plan_buf.row_loads, plan_buf.col_loads, plan_buf.head_loads,
-                                       stream=side)
-            dbsp.dbsp_plan_lpt(plan_buf.row_loads.view(-1), n_workers, plan_buf.worker_of,
-                               plan_buf.worker_offsets, plan_buf.worklist, plan_buf.worker_loads, stream=side)
-    stream.wait_stream(side)
-    for _ in range(args.warmup):
-        flush.zero_()
-        graph.replay()
-    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     clocks = ClockSampler(local)
     if rank == 0:
@@ -372,31 +360,14 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()  # L2 flush, outside the timed events
-        ev[i][0].record(stream)
-        graph.replay()
-        ev[i][2].record(stream)
+    pipelined(args.steps, ev)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    # breakdown (not part of the value): the same kernels launched from the host, with an
-    # event between the plan and the attention kernel
-    for i in range(args.steps):
-        flush.zero_()
-        step(ev[i])
-    torch.cuda.synchronize(dev)
-    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    plan_ms = []
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        graph_lp.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    plan_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    attn_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    side_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]  # loads + plan beside it
     total_s = sum(step_ms) / 1e3
     total_s = max_over_ranks(total_s, world, dev)
     t = timing.view(n_workers, 3).cpu().numpy()
@@ -406,6 +377,46 @@ def run_gpu(args):
     status = dbsp.dbsp_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
+
+    # breakdown (not part of the value): the serial step, one CUDA graph of the three
+    # launches on every SM (each kernel may start its prologue while the previous one
+    # finishes), and its mask loads + plan alone
+    plan_buf = P.alloc_plan(w.B, w.H, w.nQ, w.nK, n_sm, dev)
+    timing_sm = torch.zeros(3 * n_sm, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    graph_lp = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        loads_plan(plan_buf, n_sm, side)
+        attention(plan_buf, n_sm, side, timing_sm)
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            loads_plan(plan_buf, n_sm, side)
+            attention(plan_buf, n_sm, side, timing_sm)
+        with torch.cuda.graph(graph_lp, stream=side):
+            loads_plan(plan_buf, n_sm, side)
+    stream.wait_stream(side)
+
+    def graph_ms(g):
+        for _ in range(3):
+            flush.zero_()
+            g.replay()
+        ts = []
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+
+    serial_ms = graph_ms(graph)
+    plan_ms = graph_ms(graph_lp)
+    status = dbsp.dbsp_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the serial step")
 
     # end to end through the public API, host (pinned) buffers in and out
     q_h, k_h, v_h = (x.cpu().pin_memory() for x in (q, k, v))
@@ -419,7 +430,7 @@ def run_gpu(args):
     # its own inputs in and its own result out; the inputs of a step (201 MB) are larger
     # than L2, so no flush is needed between steps.
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    bufs = [dict(q=q, k=k, v=v, mask=mask, out=out, lse=lse, plan=plan_buf)]
+    bufs = [dict(q=q, k=k, v=v, mask=mask, out=out, lse=lse, plan=P.alloc_plan(w.B, w.H, w.nQ, w.nK, n_workers, dev))]
     bufs.append(dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v),
                      mask=torch.empty_like(mask), out=torch.empty_like(out), lse=torch.empty_like(lse),
                      plan=P.alloc_plan(w.B, w.H, w.nQ, w.nK, n_workers, dev)))
@@ -485,8 +496,12 @@ def run_gpu(args):
         "sm_skew": skew,
         "blocks_per_worker": {"min": int(blocks_per_worker.min()), "max": int(blocks_per_worker.max()),
                               "mean": float(blocks_per_worker.mean())},
-        "loads_plus_plan_us": 1e3 * statistics.mean(plan_ms),
         "attn_us": 1e6 * attn_avg_s,
+        "loads_plus_plan_beside_attn_us": 1e3 * statistics.mean(side_ms),
+        "serial_step": {"value": flop / (statistics.mean(serial_ms) / 1e3) / 1e12, "unit": UNIT,
+                        "ms_per_step": statistics.mean(serial_ms), "n_workers": n_sm,
+                        "how": "one CUDA graph of the mask-loads, LPT-plan and attention launches on every SM"},
+        "loads_plus_plan_us": 1e3 * statistics.mean(plan_ms),
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak, "traffic": attn_traffic(),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
@@ -495,7 +510,8 @@ def run_gpu(args):
         "e2e": {"value": total_flop / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "pinned host inputs in and results out every step through the public API, "
-                       "double-buffered on three streams (step i+1 copies in while step i computes)"},
+                       "double-buffered on three streams (step i+1 copies in while step i's loads, plan "
+                       "and attention run)"},
         "gpu_launches": 3 * args.steps,
         "wall_s_timed": wall,
         "clocks": clk,
@@ -880,7 +896,7 @@ def main():
     ap.add_argument("--impl", choices=["dbsp", "reference"], default="dbsp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workers", type=int, default=0,
-                    help="LPT workers of the reference arm (default: the GPU's SM count, else 152)")
+                    help="LPT workers of the reference arm (default: the GPU arm's, SM count - 1)")
     ap.add_argument("--suite", action="store_true", help="one line per workload, every kernel timed alone")
     ap.add_argument("--workloads", default="", help="comma-separated workload names for --suite")
     ap.add_argument("--profile-kernels", action="store_true",
@@ -890,7 +906,7 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         if args.workers <= 0:
-            args.workers = gpu_sm_count(152)
+            args.workers = attention_workers(gpu_sm_count(152))
         return run_reference(args)
     if args.suite:
         return run_suite(args)

@@ -115,6 +115,63 @@ def attention(q, k, v, mask, block, causal, p, out=None, lse=None, scale=0.0, ct
     return out, lse
 
 
+class PipelinedSteps:
+    """Consecutive batches with the next batch's mask loads and plan hidden behind the
+    current batch's attention.
+
+    The attention kernel fills every SM it runs on (one persistent CTA per SM holds the
+    whole register file), so a plan launched beside it would find no room. Here the
+    attention runs on ``n_workers`` = SM count - 1 workers and the remaining SM takes the
+    mask loads and the LPT plan of the next batch meanwhile, on a side stream, into the
+    second of two plan buffers. ``prime`` plans the first batch; each ``step`` then runs
+    one batch's attention on ``stream`` and plans the next one beside it. The plan waits
+    for everything enqueued on ``stream`` before the step (so it never overwrites a plan
+    that an earlier attention still reads), and ``stream`` waits for the plan at the end
+    of the step. Results are those of ``plan`` + ``attention`` on each batch.
+    """
+
+    def __init__(self, B, H, nQ, nK, device, n_workers=None, causal_loads=False):
+        self.n_workers = n_workers or max(1, default_workers(device) - 1)
+        self.plans = [alloc_plan(B, H, nQ, nK, self.n_workers, device) for _ in range(2)]
+        self.causal_loads = causal_loads
+        self._side = torch.cuda.Stream(device, priority=0)
+        self._cur = 0
+
+    def _plan(self, mask, p, stream):
+        plan(mask, self.n_workers, out=p, stream=stream, causal=self.causal_loads)
+
+    def prime(self, mask, stream=None):
+        """Plans the first batch (on ``stream``)."""
+        self._plan(mask, self.plans[self._cur], stream or torch.cuda.current_stream(mask.device))
+
+    def step(self, q, k, v, mask, block, causal, next_mask=None, out=None, lse=None, scale=0.0,
+             cta_timing=None, stream=None, events=None):
+        """Attention of the primed batch (``mask`` must be the mask it was planned from)
+        beside the loads and plan of ``next_mask`` (none when it is None). ``events``, if
+        given, are four CUDA events recorded at the step's start, the attention's end (both
+        on ``stream``), the plan's end (side stream) and the step's end (``stream``).
+        Returns (out, lse)."""
+        st = stream or torch.cuda.current_stream(q.device)
+        e = events or [torch.cuda.Event() for _ in range(4)]
+        e[0].record(st)
+        B, H, S, d = q.shape
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+        attention(q, k, v, mask, block, causal, self.plans[self._cur], out=out, lse=lse, scale=scale,
+                  cta_timing=cta_timing, stream=st)
+        e[1].record(st)
+        self._side.wait_event(e[0])
+        if next_mask is not None:
+            self._plan(next_mask, self.plans[1 - self._cur], self._side)
+        e[2].record(self._side)
+        st.wait_event(e[2])
+        e[3].record(st)
+        self._cur = 1 - self._cur
+        return out, lse
+
+
 def attention_partial(q, k, v, mask, block, causal, p, o_part, m_part, l_part, scale=0.0, stream=None):
     """Partial-mode attention (one KV shard, expressed by ``mask``) into caller buffers."""
     dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, block, causal, p.worker_offsets, p.worklist,

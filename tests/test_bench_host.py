@@ -73,14 +73,16 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
-    # the same config object as the GPU arm's line (152 workers without a GPU)
+    # the same config object as the GPU arm's line (152 SMs assumed without a GPU, one of
+    # them kept for the next batch's loads and plan)
     sys.path.insert(0, ROOT)
     import bench
     from load_balancing_gb300 import workloads as W
 
     w = W.WORKLOADS[bench.WORKLOAD]
     mask_np = W.make_mask(w)
-    assert d["config"] == bench.bench_config(w, 152, bench.dense_blocks(mask_np, w.causal))
+    assert d["config"] == bench.bench_config(w, bench.attention_workers(152), bench.dense_blocks(mask_np, w.causal))
+    assert d["config"]["n_workers"] == 151
 
 
 def test_reference_arm_nonzero_rank_exits_quietly():
