@@ -540,6 +540,11 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // warp (split 16-lane TMEM shape): thread t < 16 holds columns [0, BLOCK/2) of S and
 // [0, D/2) of O for row t, thread t + 16 the other halves. Row maxima and row sums are
 // combined with one shuffle, so the softmax warps never wait on one another.
+#ifndef DBSP_DEFER_RELEASE
+#define DBSP_DEFER_RELEASE 1
+#endif
+constexpr int kDeferRelease = DBSP_DEFER_RELEASE;  // blocks of P stored before a Q buffer's release
+
 template <int BLOCK, int D, bool UNITS>
 __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem, uint32_t data, const CUtensorMap* to) {
   using C = Cfg<BLOCK, D>;
@@ -555,6 +560,16 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem, uint32_
   const bool partial = p.o_part != nullptr;
   const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
   uint32_t items = 0, G = 0;
+  // An output tile's TMA store reads its Q buffer for a while after issue; the releaser
+  // waits for that read, and releases the buffer, only after it has stored the P of the
+  // next kDeferRelease blocks (or at its next epilogue), so that the wait does not hold
+  // back the next item's first PV. Lane 0 of the releaser warp, which issued the store.
+  int pend_qs = -1, pend_left = 0;
+  auto release_pending = [&]() {
+    bulk_wait_read_all();
+    mbar_arrive(smem_u32(&c->q_empty[pend_qs]));
+    pend_qs = -1;
+  };
   bool ok = true;
   while (ok) {
     const uint32_t slot = items & 1;
@@ -649,9 +664,13 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem, uint32_
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&c->p_full[b]));
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&c->p_full[b]));
+        if (pend_qs >= 0 && --pend_left == 0) release_pending();
+      }
     }
     if (!ok) break;
+    if (lane == 0 && pend_qs >= 0) release_pending();  // an item shorter than the deferral
     l += __shfl_xor_sync(0xffffffffu, l, 16);  // row sum over both halves
     // epilogue: wait for the last PV of this item; the next item's first PV waits for
     // these warps' P, which they store only after the reads below
@@ -712,11 +731,15 @@ __device__ void run_softmax(const AttnParams& p, Ctrl* c, uint32_t tmem, uint32_
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) tma_store_2d(to, qbuf + cc * C::kChunk128, cc * 64, row0);
         bulk_commit_group();
-        bulk_wait_read_all();
+        pend_qs = (int)qs;
+        pend_left = kDeferRelease;
+        if (kDeferRelease == 0) release_pending();
+      } else {
+        mbar_arrive(smem_u32(&c->q_empty[qs]));
       }
-      mbar_arrive(smem_u32(&c->q_empty[qs]));
     }
   }
+  if (lane == 0 && pend_qs >= 0) release_pending();
   if (lane == 0) bulk_wait_all();  // the output stores this warp issued are complete
 }
 
