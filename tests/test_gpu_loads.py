@@ -43,7 +43,10 @@ def test_workload_masks(built_library, cuda_device, name):
                                    (1, 1, 2048, 4096), (1, 1, 131072, 16), (1, 1, 3, 4112),
                                    # 8 bands of 188 rows per head, 6 stages of 32 rows each, the
                                    # last band shorter and ragged
-                                   (2, 2, 1500, 512)])
+                                   (2, 2, 1500, 512),
+                                   # several 1 MB heads of 8 ranks; rows of 65 units whose stages
+                                   # end ragged (15 rows per stage)
+                                   (2, 3, 1024, 1024), (1, 5, 1000, 1040)])
 @pytest.mark.parametrize("density", [0.0, 0.3, 1.0])
 def test_random_masks(built_library, cuda_device, shape, density):
     rng = np.random.default_rng(hash((shape, density)) % 2**32)
@@ -89,12 +92,13 @@ def test_kv_block_loads(built_library, cuda_device, name):
 
 
 @pytest.mark.parametrize("shape", [(1, 2, 16, 16), (2, 3, 64, 64), (1, 1, 1024, 1024), (1, 2, 300, 300),
-                                   (1, 1, 4112, 4112), (1, 1, 33, 33)])
+                                   (1, 1, 4112, 4112), (1, 1, 33, 33), (1, 2, 2048, 2048)])
 def test_causal_loads_count_only_blocks_on_or_below_the_diagonal(built_library, cuda_device, shape):
     """dbsp_block_mask_loads_causal on masks that are NOT clipped to the diagonal equals
     the oracle's loads of the same masks clipped to it (6D notes §2.3: the blocks after
     a Q block's diagonal are skipped): streamed rows (16 and 64 KV blocks, 1024 with the
-    unrolled path), byte rows (300, 33) and 16-byte register rows (4112)."""
+    unrolled path, 2048 over 8 ranks of 256 rows), byte rows (300, 33) and 16-byte
+    register rows (4112)."""
     from load_balancing_gb300 import dbsp
 
     rng = np.random.default_rng(sum(shape))
