@@ -161,6 +161,77 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlPoller:
+    """SM clock and clock-event reasons read through NVML every millisecond while the
+    timed region runs (read-only queries; nothing is set). The timed region of a default
+    run lasts a few milliseconds, shorter than nvidia-smi's shortest sampling interval."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+
+        self.ok = False
+        self.samples, self.reasons = [], 0
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+
+                uuid = str(torch.cuda.get_device_properties(device).uuid)
+            except Exception:
+                pass
+            found = False
+            if uuid:
+                key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                found = nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(handle)) == 0
+            if not found:
+                found = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device.index or 0), ctypes.byref(handle)) == 0
+            if not found:
+                return
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0 else None
+            self.nv, self.handle, self.ctypes = nv, handle, ctypes
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _run(self):
+        c = self.ctypes
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.handle, 1, c.byref(mhz)) == 0:  # NVML_CLOCK_SM
+                self.samples.append(float(mhz.value))
+            if self._reason_fn(self.handle, c.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(0.001)
+
+    def start(self):
+        import threading
+
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if not self.ok or self._thread is None:
+            return None
+        self._stop.set()
+        self._thread.join(timeout=5)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for bit, n in self.REASONS.items() if self.reasons & bit),
+                "samples": len(self.samples), "source": "NVML, every 1 ms during the timed steps"}
+
+
 # ----------------------------------------------------------------------------- distributed
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
@@ -355,16 +426,21 @@ def run_gpu(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     clocks = ClockSampler(local)
+    poller = NvmlPoller(dev)
     if rank == 0:
         clocks.start()
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
+    poller.start()
     pipelined(args.steps, ev)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    nvml = poller.stop()
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
+    if clk is not None and nvml is not None:  # the in-region samples lead; nvidia-smi's around it
+        clk = dict(nvml, nvidia_smi=clk)
     step_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
     attn_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     side_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]  # loads + plan beside it
@@ -891,7 +967,7 @@ def run_kernels_once(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dbsp", "reference"], default="dbsp")
     ap.add_argument("--no-cpu-baseline", action="store_true")
