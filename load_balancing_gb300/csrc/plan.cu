@@ -564,6 +564,38 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
   }
 }
 
+// Phase 2 with a bonus above the total planning load: an item's home key, lowered by the
+// bonus, is negative and so below every other key, so every item stays at home. One warp
+// walks the stable order 32 items at a time; items with the same home take consecutive
+// ranks in that order (match_any), as the one-at-a-time greedy would place them.
+__device__ __forceinline__ void greedy_all_home(const Sorted sorted, const int32_t* __restrict__ loads,
+                                                const int32_t* __restrict__ home, int bc, int ic, int n, int m,
+                                                int cm, int* counts, long long* final_load,
+                                                int32_t* __restrict__ worker_of) {
+  const int lane = threadIdx.x & 31;
+  for (int p = lane; p < m; p += 32) {
+    counts[p] = 0;
+    final_load[p] = 0;
+  }
+  __syncwarp();
+  for (int base = 0; base < n; base += 32) {
+    const int t = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, t < n);
+    if (t < n) {
+      const int i = sorted[t];
+      const int h = home[i];
+      const unsigned peers = __match_any_sync(active, h);
+      const unsigned below = peers & ((1u << lane) - 1u);
+      worker_of[i] = h + cm * (counts[h] + __popc(below));
+      atomicAdd(reinterpret_cast<unsigned long long*>(&final_load[h]),
+                (unsigned long long)((long long)loads[i] * bc + ic));
+      __syncwarp(active);
+      if (below == 0) counts[h] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     const int32_t* __restrict__ loads, const int32_t* __restrict__ home, int n_max, const int32_t* n_dev, int m,
@@ -780,7 +812,9 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   const int wpb = (m + 31) >> 5;
   const bool ring = staged && ring_R <= kRingMax && (long long)ring_R * wpb <= kRingWords &&
                     (long long)n * wmax < (1LL << 31);
-  if (counting && (home == nullptr || bonus == 0) && ring) {
+  if (home != nullptr && bonus > 0 && (unsigned long long)bonus > sh.total_load) {
+    if (tid < 32) greedy_all_home(sorted, loads, home, bc, ic, n, m, cm, counts, final_load, worker_of);
+  } else if (counting && (home == nullptr || bonus == 0) && ring) {
     if (!greedy_sorted(loads, sorted.smem, sload, bin_end, nbins, max_load, n, m, cm, bc, ic, ring_R,
                        reinterpret_cast<uint32_t*>(dyn + kRingOff), reinterpret_cast<int*>(dyn + kPreOff),
                        reinterpret_cast<int*>(dyn + kCntOff), reinterpret_cast<int*>(dyn + kLwOff),

@@ -73,6 +73,29 @@ def test_static_home_schedule_and_huge_bonus(built_library, cuda_device):
         _assert_same(_plan(loads, m, home, bonus), OP.lpt_plan(loads, m, home, bonus))
 
 
+@pytest.mark.parametrize("m", [1, 7, 152, 1024])
+def test_bonus_above_total_load_keeps_every_item_home(built_library, cuda_device, m):
+    """A bonus above the total load makes every lowered home key the smallest, so every
+    item stays at home, ranked by the LPT order (the plan takes a one-warp path for it);
+    a bonus equal to the total load still takes the general greedy. Both bit-exact."""
+    rng = np.random.default_rng(21 + m)
+    n = 3000
+    loads = rng.integers(0, 80, n)
+    home = rng.integers(0, m, n)
+    total = int(loads.sum())
+    for bonus in (total + 1, 1 << 20):
+        got = _plan(loads, m, home, bonus)
+        _assert_same(got, OP.lpt_plan(loads, m, home, bonus))
+        np.testing.assert_array_equal(got["worker_of"], home)
+    _assert_same(_plan(loads, m, home, total), OP.lpt_plan(loads, m, home, total))
+    # more items than the staged order holds: the order lives in the worklist
+    n2 = 50000
+    loads2 = rng.integers(1, 3000, n2)
+    home2 = rng.integers(0, m, n2)
+    got = _plan(loads2, m, home2, 1 << 30)
+    _assert_same(got, OP.lpt_plan(loads2, m, home2, 1 << 30))
+
+
 def test_large_loads_take_comparison_sort(built_library, cuda_device):
     rng = np.random.default_rng(4)
     loads = rng.integers(0, 5_000_000, 3000)
