@@ -19,16 +19,16 @@
 //            shared-memory histogram, its stable scatter done by one warp with
 //            match_any (or rank-by-comparison for n <= 16384 with large loads);
 //   phase 2  the greedy.
-//            Without a bonus (whole CTA) it goes one RUN of equal loads w at a time, in
-//            batches: with the workers' keys sorted ascending in A, every key
-//            below A[0] + (w << 11) is taken in order by the next items of the
-//            run -- each re-keyed worker (key + (w << 11)) is above all of
-//            them, so the one-at-a-time greedy picks exactly this sequence --
-//            then the re-keyed batch is merged back into A (binary searches, one
-//            element per thread). With a bonus (one warp) the key of item i's home worker is lowered by the
-//            bonus for that choice only, so items go one at a time: every lane
-//            keeps the keys of workers lane, lane+32, ... in registers and the
-//            warp minimum takes two redux.sync (high word, then low word).
+//            Without a bonus (whole CTA) it goes in batches over the workers' keys sorted
+//            ascending in A: the next items take A[0], A[1], ... while A[j] stays below
+//            A[0] + W(s + j), exactly the one-at-a-time greedy's picks, then A is rebuilt
+//            by a counting sort over a ring of load buckets (when the loads are staged
+//            and small), else the re-keyed keys are merged back by binary searches.
+//            With a bonus (one warp) the key of item i's home worker is lowered by the
+//            bonus for that choice only, so items go one at a time: every lane keeps the
+//            keys of workers lane, lane+32, ... in registers and one warp minimum (two
+//            for 64-bit keys) decides an item. A bonus above the total load keeps every
+//            item at home: one warp ranks each worker's items in the stable order.
 //            worker_of[i] temporarily holds worker + cm * (rank within worker), cm = 1024
 //            (or m when ranks could reach 2^21);
 //   phase 3  CSR offsets by a block scan of the per-worker counts, then the
