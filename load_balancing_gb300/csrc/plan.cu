@@ -13,7 +13,7 @@
 // CTA of 256 threads:
 //
 //   phase 0  check loads and home, find the load range; when n <= 45056 and every
-//            load <= 4095 the loads are staged in shared memory as uint16
+//            load <= 2047 the loads are staged in shared memory as uint16
 //            ("staged" path), otherwise the kernel works from global memory;
 //   phase 1  the stable order (load desc, id asc): a counting sort through a
 //            shared-memory histogram, its stable scatter done by one warp with
