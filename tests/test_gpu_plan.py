@@ -64,6 +64,35 @@ def test_random_instances_with_bonus(built_library, cuda_device, m):
         _assert_same(_plan(loads, m, home, bonus), OP.lpt_plan(loads, m, home, bonus))
 
 
+@pytest.mark.parametrize("name", ["llm", "video", "sharded"])
+def test_plan_reuse_with_bonus(built_library, cuda_device, name):
+    """The plan-reuse scenario (db-SP blog, scenario 2, third bullet): the next mask flips
+    2 % of the blocks and its plan takes the previous plan as home. Bonuses from 1 up to
+    past the loads' spread, bit-exact."""
+    w = W.WORKLOADS[name]
+    mask0 = W.make_mask(w)
+    mask1 = W.perturb_mask(mask0, 0.02, 1, w.causal)
+    row0 = OL.block_mask_loads(mask0)[0].reshape(-1)
+    row1 = OL.block_mask_loads(mask1)[0].reshape(-1)
+    m = torch.cuda.get_device_properties(0).multi_processor_count - 1
+    home = np.asarray(OP.lpt_plan(row0, m)["worker_of"])
+    for bonus in (1, 2, 4, 8, 32, 100, 1000):
+        _assert_same(_plan(row1, m, home, bonus), OP.lpt_plan(row1, m, home, bonus))
+
+
+@pytest.mark.parametrize("m", [2, 5, 64, 151, 1024])
+def test_batched_bonus_random_homes(built_library, cuda_device, m):
+    """Random homes, zero loads at the tail, bonuses small and large against the loads,
+    from a handful of items to 9,000."""
+    rng = np.random.default_rng(100 + m)
+    for n in (7, 500, 4096, 8192, 9000):
+        loads = rng.integers(0, 60, n)
+        loads[rng.random(n) < 0.05] = 0
+        home = rng.integers(0, m, n)
+        for bonus in (1, 3, 17, 90):
+            _assert_same(_plan(loads, m, home, bonus), OP.lpt_plan(loads, m, home, bonus))
+
+
 def test_static_home_schedule_and_huge_bonus(built_library, cuda_device):
     rng = np.random.default_rng(9)
     n, m = 4096, 148
