@@ -393,7 +393,7 @@ def run_gpu(args):
     n_workers = attention_workers(n_sm)
     # the timed step: batch i's attention on n_workers SMs beside batch i+1's mask loads and
     # plan on the remaining one (two plan buffers, kept by PipelinedSteps)
-    pipe = P.PipelinedSteps(w.B, w.H, w.nQ, w.nK, dev, n_workers=n_workers)
+    pipe = P.PipelinedSteps(w.B, w.H, w.nQ, w.nK, dev, causal=w.causal, n_workers=n_workers)
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
     timing = torch.zeros(3 * n_workers, dtype=torch.int64, device=dev)

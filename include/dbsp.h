@@ -125,6 +125,26 @@ DBSP_API int dbsp_shard_masks(const uint8_t* mask, int B, int H, int nQ, int nK,
                               int n_shards, uint8_t* out, void* stream);
 
 /*
+ * Dense-block lists.  [db-SP blog, scenario 2, first bullet]: a Q-block row's load is
+ * its dense blocks; this lists them. For every row r = (b*H + h)*nQ + qb of the mask,
+ * the KV-block indices of its dense blocks in ascending order go to
+ * cols[r*nK + 0 .. counts[r] - 1] (with causal != 0 only the blocks on or below the
+ * diagonal, the ones causal attention computes). Input for the attention producers
+ * (dbsp_block_sparse_attn_fwd_listed), which then read an item's tiles from here
+ * instead of scanning its mask row.
+ *
+ *   mask    uint8 [B, H, nQ, nK]; any non-zero byte is a dense block.
+ *   counts  int32 [B*H*nQ] out: the row's dense blocks (= its row load).
+ *   cols    uint16 [B*H*nQ, nK] out, 2-byte aligned; entries past counts[r] are not
+ *           written.
+ * Requires B, H, nQ, nK >= 1, B*H*nQ*nK < 2^31, nK <= 65536 (else DBSP_ERR_UNSUPPORTED)
+ * and nQ == nK with causal != 0. One warp per row, 16-byte loads when nK % 16 == 0 and
+ * the mask is 16-byte aligned, byte loads otherwise. Ownership: caller-owned buffers.
+ */
+DBSP_API int dbsp_dense_block_lists(const uint8_t* mask, int B, int H, int nQ, int nK, int causal,
+                                    int32_t* counts, uint16_t* cols, void* stream);
+
+/*
  * LPT plan with stay-in-place bonus.  [db-SP blog, scenario 1]: repeatedly give
  * the largest remaining item to the currently least-loaded worker (LPT).
  * [db-SP blog, scenario 2, third bullet]: an item placed on its original worker
@@ -258,6 +278,27 @@ DBSP_API int dbsp_block_sparse_attn_fwd(const void* q, const void* k, const void
                                void* out, float* lse,
                                float* o_part, float* m_part, float* l_part,
                                int64_t* cta_timing, void* stream);
+
+/*
+ * dbsp_block_sparse_attn_fwd with the dense-block lists of dbsp_dense_block_lists: the
+ * producer warps read each item's dense count and KV-block indices from dense_n and
+ * dense_cols (same layout) instead of scanning its mask row, and fetch the next item's
+ * entry while the current item's tiles go out; the mask is not read. Same arguments,
+ * modes and results otherwise (bit-identical output). The lists must be those of the
+ * same mask, built with the same causal flag. A count outside [0, limit] or an index at
+ * or past the row's limit (nK, or qb + 1 when causal) sets DBSP_ERR_INVALID_ARG on the
+ * device; the row is then written as empty, or the tile replaced by block 0.
+ *   dense_n     int32 [B*H*nQ]; dense_cols uint16 [B*H*nQ, nK], 2-byte aligned.
+ */
+DBSP_API int dbsp_block_sparse_attn_fwd_listed(const void* q, const void* k, const void* v,
+                                      const uint8_t* mask, int B, int H, int S, int d, int block,
+                                      int causal, float scale,
+                                      const int32_t* worker_offsets, const int32_t* worklist,
+                                      int n_workers, const int32_t* dense_n,
+                                      const uint16_t* dense_cols,
+                                      void* out, float* lse,
+                                      float* o_part, float* m_part, float* l_part,
+                                      int64_t* cta_timing, void* stream);
 
 /*
  * Block-sparse attention forward over a worklist of units (dbsp_split_plan).  Each

@@ -110,6 +110,10 @@ struct AttnParams {
   float* o_piece;
   float* m_piece;
   float* l_piece;
+  // dense-block lists (optional): row r's dense KV blocks within the causal limit are
+  // dense_cols[r * nK + 0 .. dense_n[r] - 1], ascending
+  const int32_t* dense_n;
+  const uint16_t* dense_cols;
 };
 
 template <int BLOCK, int D>
@@ -409,6 +413,182 @@ __device__ void run_producer(int which, const CUtensorMap* tq, const CUtensorMap
       }
       ok = __shfl_sync(kAll, ok, 0);
       if constexpr (UNITS) past = __shfl_sync(kAll, past, 0);
+      __syncwarp();
+    }
+  }
+  // teardown: let every copy this warp started land before shared memory goes away
+  if (lane == 0) {
+    for (uint32_t k = t_cnt > kstages ? t_cnt - kstages : 0; k < t_cnt; ++k) {
+      if (which == 0) drain_bar(smem_u32(&c->k_full[k % kstages]), (k / kstages) & 1);
+      else drain_bar(smem_u32(&c->p_full[k % kSBufs]), (k / kSBufs) & 1);
+    }
+    for (uint32_t k = q_cnt > (uint32_t)kQBufs ? q_cnt - kQBufs : 0; k < q_cnt; ++k)
+      drain_bar(smem_u32(&c->q_full[k % kQBufs]), (k / kQBufs) & 1);
+  }
+  __syncwarp();
+}
+
+// Producer warp `which` over precomputed dense-block lists: the schedule of run_producer,
+// but an item's dense count and columns are read from the lists instead of its mask row,
+// and the next item's worklist entry, count and first 32 columns load while the current
+// item's tiles go out. A count outside [0, limit] or a column at or past the limit sets
+// DBSP_ERR_INVALID_ARG; the row is then treated as empty, or the tile as block 0, so that
+// both producers and the MMA issuers stay in step.
+template <int BLOCK, int D>
+__device__ void run_producer_listed(int which, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                    const AttnParams& p, Ctrl* c, uint8_t* data) {
+  using C = Cfg<BLOCK, D>;
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int nK = p.nK;
+  int begin = p.offsets[blockIdx.x], end = p.offsets[blockIdx.x + 1];
+  if (begin < 0 || end < begin) {
+    if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+    begin = end = 0;
+  }
+  uint32_t item_cnt = 0, q_cnt = 0, t_cnt = 0;
+  const uint32_t kstages = which == 0 ? kKStages : kVStages;
+  uint64_t* done = which == 0 ? c->s_full : c->pv_done;
+  const uint32_t ring = smem_u32(data + (which == 0 ? C::kKOff : C::kVOff));
+  const CUtensorMap* map = which == 0 ? tk : tv;
+  auto valid_item = [&](int u) { return u >= 0 && u < p.n_items; };
+  auto list = [&](int u) { return p.dense_cols + (long long)u * nK; };
+  int u_cur = begin < end ? __ldg(p.worklist + begin) : -1;
+  int u_nxt = begin + 1 < end ? __ldg(p.worklist + begin + 1) : -1;
+  int n_cur = 0;
+  uint32_t c_cur = 0;
+  if (valid_item(u_cur)) {
+    n_cur = __ldg(p.dense_n + u_cur);
+    c_cur = lane < nK ? __ldg(list(u_cur) + lane) : 0u;
+  }
+  bool ok = true;
+  for (int idx = begin; idx <= end && ok; ++idx) {
+    const int u = u_cur;
+    const int n_in = n_cur;
+    const uint32_t cw0 = c_cur;
+    // the next entry's count and first columns, and the entry after it (used next time)
+    int n_nx = 0;
+    uint32_t c_nx = 0u;
+    if (valid_item(u_nxt)) {
+      n_nx = __ldg(p.dense_n + u_nxt);
+      c_nx = lane < nK ? __ldg(list(u_nxt) + lane) : 0u;
+    }
+    const int u_nx2 = idx + 2 < end ? __ldg(p.worklist + idx + 2) : -1;
+    u_cur = u_nxt;
+    n_cur = n_nx;
+    c_cur = c_nx;
+    u_nxt = u_nx2;
+
+    int item = -1;
+    if (idx < end) {
+      item = u;
+      if (!valid_item(item)) {
+        if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+        continue;
+      }
+    }
+    int n = 0, limit = 0;
+    long long kv_row0 = 0;
+    if (item >= 0) {
+      kv_row0 = (long long)(item / p.nQ) * p.S;
+      limit = p.causal ? min(nK, item % p.nQ + 1) : nK;
+      n = n_in;
+      if (n < 0 || n > limit) {
+        if (lane == 0 && which == 0) dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+        n = 0;
+      }
+    }
+    if (which == 0 && item >= 0 && n == 0) {
+      // an item without dense blocks never reaches the MMA issuers or the softmax: this
+      // warp writes its rows itself (partial mode: m = -inf, l = 0; final: O = 0, LSE = -inf)
+      const long long row0 = (long long)(item / p.nQ) * p.S + (long long)(item % p.nQ) * BLOCK;
+      if (p.o_part) {
+        for (int r = lane; r < BLOCK; r += 32) {
+          p.m_part[row0 + r] = -INFINITY;
+          p.l_part[row0 + r] = 0.f;
+        }
+      } else {
+        uint4* o = reinterpret_cast<uint4*>(p.out + row0 * D);
+        for (int i = lane; i < BLOCK * D / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse)
+          for (int r = lane; r < BLOCK; r += 32) p.lse[row0 + r] = -INFINITY;
+      }
+      continue;
+    }
+    if (which == 0) {  // publish the item
+      int diag = 0;
+      if (item >= 0 && p.causal) {  // the row's last dense block is the diagonal one
+        const int last = n <= 32 ? __shfl_sync(kAll, (int)cw0, n - 1) : (int)__ldg(list(item) + n - 1);
+        diag = last == item % p.nQ;
+      }
+      const uint32_t slot = item_cnt & 1, su = item_cnt >> 1;
+      if (lane == 0) {
+        ok = wait_bar(c, smem_u32(&c->item_empty[slot]), (su & 1) ^ 1, p.err);
+        if (ok) {
+          c->item_id[slot] = item;
+          c->item_n[slot] = n;
+          c->item_diag[slot] = diag;
+          c->item_slot[slot] = -1;
+          mbar_arrive(smem_u32(&c->item_full[slot]));
+        }
+      }
+      ok = __shfl_sync(kAll, ok, 0);
+      ++item_cnt;
+      if (!ok || item < 0) break;
+      if (lane == 0) {  // the Q tile of this item
+        const uint32_t qs = q_cnt % kQBufs, qu = q_cnt / kQBufs;
+        ok = wait_bar(c, smem_u32(&c->q_empty[qs]), (qu & 1) ^ 1, p.err);
+        if (ok) {
+          const uint32_t qf = smem_u32(&c->q_full[qs]);
+          mbar_arrive_expect_tx(qf, C::kTx);
+          const int qrow = (int)(kv_row0 + (long long)(item % p.nQ) * BLOCK);
+          const uint32_t dst = smem_u32(data) + qs * C::kQBytes;
+#pragma unroll
+          for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kChunk128, tq, ch * 64, qrow, qf);
+        }
+        ++q_cnt;
+      }
+      ok = __shfl_sync(kAll, ok, 0);
+      if (!ok) break;
+    } else if (item < 0) {
+      break;
+    }
+    // the dense K (or V) tiles of the item, in block order, 32 columns at a time
+    for (int k0 = 0; k0 < n && ok; k0 += 32) {
+      const uint32_t cw = k0 == 0 ? cw0 : (k0 + lane < n ? (uint32_t)__ldg(list(item) + k0 + lane) : 0u);
+      c->scan_bits[which][lane] = (uint16_t)cw;
+      __syncwarp();
+      if (lane == 0) {
+        const int cnt = min(32, n - k0);
+        for (int t = 0; t < cnt && ok; ++t) {
+          int col = c->scan_bits[which][t];
+          if (col >= limit) {
+            dbsp::report(p.err, DBSP_ERR_INVALID_ARG);
+            col = 0;
+          }
+          const uint32_t s = t_cnt % kstages;
+          if (t_cnt >= kstages) {
+            const uint32_t prev = t_cnt - kstages;
+            ok = wait_bar(c, smem_u32(&done[prev % kSBufs]), (prev / kSBufs) & 1, p.err);
+          }
+#ifdef DBSP_WAIT_TEST
+          if (ok && which == 1 && blockIdx.x == 0 && t_cnt == 0) {  // the left-out tile
+            ++t_cnt;
+            continue;
+          }
+#endif
+          if (ok) {
+            const uint32_t f = smem_u32(which == 0 ? &c->k_full[s] : &c->p_full[t_cnt % kSBufs]);
+            mbar_arrive_expect_tx(f, C::kTx);
+            const uint32_t dst = ring + s * C::kTileBytes;
+            const int row = (int)(kv_row0 + (long long)col * BLOCK);
+#pragma unroll
+            for (int ch = 0; ch < D / 64; ++ch) tma_load_2d(dst + ch * C::kTileChunk, map, ch * 64, row, f);
+            ++t_cnt;
+          }
+        }
+      }
+      ok = __shfl_sync(kAll, ok, 0);
       __syncwarp();
     }
   }
@@ -797,7 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(
   if (warp < kSoftmaxWarp0) {
     setmaxnreg_dec<kRegsControl>();
     if (warp < 2) {
-      run_producer<BLOCK, D, UNITS>(warp, &tq, &tk, &tv, p, c, base);
+      if (!UNITS && p.dense_cols)
+        run_producer_listed<BLOCK, D>(warp, &tq, &tk, &tv, p, c, base);
+      else
+        run_producer<BLOCK, D, UNITS>(warp, &tq, &tk, &tv, p, c, base);
     } else {
       if (lane == 0) {
         if (warp == kMmaWarp) run_mma_s<BLOCK, D>(p, c, smem_u32(base), tmem);
@@ -889,6 +1072,8 @@ struct Units {
   float* o_piece;
   float* m_piece;
   float* l_piece;
+  const int32_t* dense_n = nullptr;     // dense-block lists (plain worklists only)
+  const uint16_t* dense_cols = nullptr;
 };
 
 int attn_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, int B, int H, int S, int d,
@@ -944,6 +1129,8 @@ int attn_fwd(const void* q, const void* k, const void* v, const uint8_t* mask, i
   p.o_piece = u.o_piece;
   p.m_piece = u.m_piece;
   p.l_piece = u.l_piece;
+  p.dense_n = u.dense_n;
+  p.dense_cols = u.dense_cols;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (block == 128 && d == 128) return launch_attn<128, 128>(q, k, v, p, rows, n_workers, s);
   if (block == 128 && d == 64) return launch_attn<128, 64>(q, k, v, p, rows, n_workers, s);
@@ -979,4 +1166,21 @@ extern "C" int dbsp_block_sparse_attn_fwd_units(const void* q, const void* k, co
   const Units u{unit_item, unit_pk, unit_slot, n_units, max_slots, o_piece, m_piece, l_piece};
   return attn_fwd(q, k, v, mask, B, H, S, d, block, causal, scale, worker_offsets, worklist, n_workers, out,
                   lse, nullptr, nullptr, nullptr, cta_timing, u, stream);
+}
+
+extern "C" int dbsp_block_sparse_attn_fwd_listed(const void* q, const void* k, const void* v,
+                                                 const uint8_t* mask, int B, int H, int S, int d,
+                                                 int block, int causal, float scale,
+                                                 const int32_t* worker_offsets, const int32_t* worklist,
+                                                 int n_workers, const int32_t* dense_n,
+                                                 const uint16_t* dense_cols, void* out, float* lse,
+                                                 float* o_part, float* m_part, float* l_part,
+                                                 int64_t* cta_timing, void* stream) {
+  if (!dense_n || !dense_cols || !dbsp::aligned(dense_n, 4) || !dbsp::aligned(dense_cols, 2))
+    return DBSP_ERR_INVALID_ARG;
+  Units u{nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr};
+  u.dense_n = dense_n;
+  u.dense_cols = dense_cols;
+  return attn_fwd(q, k, v, mask, B, H, S, d, block, causal, scale, worker_offsets, worklist, n_workers, out,
+                  lse, o_part, m_part, l_part, cta_timing, u, stream);
 }

@@ -435,6 +435,59 @@ __global__ void __launch_bounds__(kThreads) mask_loads_stream_kernel(
   }
 }
 
+// Dense-block lists: for every row r of the mask (B*H*nQ rows of nK blocks), the KV-block
+// indices of its dense blocks in ascending order, cols[r * nK + 0 .. counts[r] - 1] (with
+// CAUSAL only the blocks on or below the diagonal). A row takes G lanes of a warp (G a power
+// of two, 16 G columns per pass: rows of up to 512 blocks in one pass, 32 / G rows per
+// warp; longer rows a whole warp, 512 columns at a time): lane l of the row holds 16
+// columns as a bit mask, and a prefix sum over the row's lanes gives each lane where its
+// indices go.
+template <bool VEC, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads) dense_lists_kernel(const uint8_t* __restrict__ mask, long long rows,
+                                                               int nQ, int nK, int G, int32_t* __restrict__ counts,
+                                                               uint16_t* __restrict__ cols) {
+  griddep_wait();  // the mask may come from the previous grid
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / G, sl = lane % G;
+  const long long r = ((long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * (32 / G) + sub;
+  const bool live = r < rows;
+  const int limit = !live ? 0 : (CAUSAL ? min(nK, (int)(r % nQ) + 1) : nK);
+  const int warp_limit = __reduce_max_sync(0xffffffffu, limit);
+  const uint8_t* row = mask + (live ? r : 0) * nK;
+  uint16_t* out = cols + (live ? r : 0) * nK;
+  int base = 0;
+  for (int c0 = 0; c0 < warp_limit; c0 += 16 * G) {
+    const int col = c0 + 16 * sl;
+    const int rem = limit - col;
+    uint32_t bits = 0;
+    if (rem > 0) {
+      if (VEC) {
+        const uint4 x = *reinterpret_cast<const uint4*>(row + col);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) bits |= ((nonzero_byte_flags(w[k]) * 0x01020408u) >> 24) << (4 * k);
+      } else {
+        for (int t = 0; t < 16 && t < rem; ++t) bits |= (row[col + t] != 0 ? 1u : 0u) << t;
+      }
+      if (rem < 16) bits &= (1u << rem) - 1u;
+    }
+    const int cnt = __popc(bits);
+    int incl = cnt;
+    for (int o = 1; o < G; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o, G);
+      if (sl >= o) incl += y;
+    }
+    int at = base + incl - cnt;
+    while (bits) {
+      out[at++] = (uint16_t)(col + __ffs(bits) - 1);
+      bits &= bits - 1;
+    }
+    base += __shfl_sync(0xffffffffu, incl, G - 1, G);
+  }
+  if (live && sl == 0) counts[r] = base;
+}
+
 // KV-block loads summed over (b, h): thread j adds column j of every head.
 __global__ void __launch_bounds__(kThreads) kv_block_loads_kernel(const int32_t* __restrict__ col_loads,
                                                                   int groups, int nK,
@@ -572,7 +625,45 @@ int mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK, int32_t* row_l
   return DBSP_OK;
 }
 
+int dense_lists(const uint8_t* mask, int B, int H, int nQ, int nK, int causal, int32_t* counts, uint16_t* cols,
+                void* stream) {
+  if (!mask || !counts || !cols) return DBSP_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || nQ < 1 || nK < 1) return DBSP_ERR_INVALID_ARG;
+  if (causal && nQ != nK) return DBSP_ERR_INVALID_ARG;
+  if ((long long)B * H * nQ * nK >= (1LL << 31)) return DBSP_ERR_INVALID_ARG;
+  if (nK > 65536) return DBSP_ERR_UNSUPPORTED;  // indices are 16-bit
+  if (!dbsp::aligned(counts, 4) || !dbsp::aligned(cols, 2)) return DBSP_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = dbsp::check_device(&dev);
+  if (st != DBSP_OK) return st;
+  const long long rows = (long long)B * H * nQ;
+  const bool vec = (nK % 16 == 0) && dbsp::aligned(mask, 16);
+  int G = 1;  // lanes per row: 16 G columns cover min(nK, 512)
+  while (G < 32 && 16 * G < nK) G <<= 1;
+  const long long per_cta = (kThreads / 32) * (32 / G);
+  const dim3 grid((unsigned)((rows + per_cta - 1) / per_cta));
+  cudaError_t e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (vec)
+    e = causal ? dbsp::launch_overlapped(dense_lists_kernel<true, true>, grid, dim3(kThreads), 0, s, mask, rows, nQ,
+                                         nK, G, counts, cols)
+               : dbsp::launch_overlapped(dense_lists_kernel<true, false>, grid, dim3(kThreads), 0, s, mask, rows, nQ,
+                                         nK, G, counts, cols);
+  else
+    e = causal ? dbsp::launch_overlapped(dense_lists_kernel<false, true>, grid, dim3(kThreads), 0, s, mask, rows, nQ,
+                                         nK, G, counts, cols)
+               : dbsp::launch_overlapped(dense_lists_kernel<false, false>, grid, dim3(kThreads), 0, s, mask, rows, nQ,
+                                         nK, G, counts, cols);
+  if (e != cudaSuccess) return dbsp::cuda_fail(e, "launch dense_lists");
+  return DBSP_OK;
+}
+
 }  // namespace
+
+extern "C" int dbsp_dense_block_lists(const uint8_t* mask, int B, int H, int nQ, int nK, int causal,
+                                      int32_t* counts, uint16_t* cols, void* stream) {
+  return dense_lists(mask, B, H, nQ, nK, causal, counts, cols, stream);
+}
 
 extern "C" int dbsp_block_mask_loads(const uint8_t* mask, int B, int H, int nQ, int nK, int32_t* row_loads,
                                      int32_t* col_loads, int32_t* head_loads, void* stream) {

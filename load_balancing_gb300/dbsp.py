@@ -32,6 +32,7 @@ _SIGNATURES = {
     "dbsp_block_mask_loads": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "dbsp_block_mask_loads_causal": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "dbsp_shard_masks": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
+    "dbsp_dense_block_lists": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dbsp_kv_block_loads": (_i32, [_vp, _i32, _i32, _vp, _vp]),
     "dbsp_plan_lpt": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "dbsp_plan_lpt_cost": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp,
@@ -39,6 +40,9 @@ _SIGNATURES = {
     "dbsp_block_sparse_attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]),
+    "dbsp_block_sparse_attn_fwd_listed": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                                 ctypes.c_float, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp,
+                                                 _vp, _vp, _vp, _vp]),
     "dbsp_merge_partials": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp]),
     "dbsp_plan_lpt_cost_n": (_i32, [_vp, _vp, _i32, _i32, ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp, _vp,
                                     _vp]),
@@ -194,6 +198,38 @@ def dbsp_block_sparse_attn_fwd(q, k, v, mask, block, causal, worker_offsets, wor
         _ptr(l_part, torch.float32, "l_part", True), _ptr(cta_timing, torch.int64, "cta_timing", True),
         _stream(stream))
     _check(st, "dbsp_block_sparse_attn_fwd")
+
+
+def dbsp_dense_block_lists(mask, causal=False, counts=None, cols=None, stream=None):
+    """Dense-block lists of every mask row: counts int32 [B,H,nQ], cols int16 [B,H,nQ,nK]
+    (the KV-block indices as 16-bit words, ascending; entries past the count unwritten)."""
+    B, H, nQ, nK = mask.shape
+    if counts is None:
+        counts = torch.empty((B, H, nQ), dtype=torch.int32, device=mask.device)
+    if cols is None:
+        cols = torch.empty((B, H, nQ, nK), dtype=torch.int16, device=mask.device)
+    st = library().dbsp_dense_block_lists(
+        _ptr(mask, torch.uint8, "mask"), B, H, nQ, nK, int(bool(causal)), _ptr(counts, torch.int32, "counts"),
+        _ptr(cols, torch.int16, "cols"), _stream(stream))
+    _check(st, "dbsp_dense_block_lists")
+    return counts, cols
+
+
+def dbsp_block_sparse_attn_fwd_listed(q, k, v, mask, block, causal, worker_offsets, worklist, n_workers,
+                                      dense_n, dense_cols, out=None, lse=None, o_part=None, m_part=None,
+                                      l_part=None, scale=0.0, cta_timing=None, stream=None):
+    """dbsp_block_sparse_attn_fwd reading each item's dense blocks from dbsp_dense_block_lists."""
+    B, H, S, d = q.shape
+    st = library().dbsp_block_sparse_attn_fwd_listed(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+        _ptr(mask, torch.uint8, "mask"), B, H, S, d, block, int(bool(causal)), float(scale),
+        _ptr(worker_offsets, torch.int32, "worker_offsets"), _ptr(worklist, torch.int32, "worklist"),
+        n_workers, _ptr(dense_n, torch.int32, "dense_n"), _ptr(dense_cols, torch.int16, "dense_cols"),
+        _ptr(out, torch.bfloat16, "out", True), _ptr(lse, torch.float32, "lse", True),
+        _ptr(o_part, torch.float32, "o_part", True), _ptr(m_part, torch.float32, "m_part", True),
+        _ptr(l_part, torch.float32, "l_part", True), _ptr(cta_timing, torch.int64, "cta_timing", True),
+        _stream(stream))
+    _check(st, "dbsp_block_sparse_attn_fwd_listed")
 
 
 def dbsp_merge_partials(o_parts, m_parts, l_parts, out, lse=None, stream=None):

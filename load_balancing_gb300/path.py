@@ -101,17 +101,31 @@ def shard_masks_from_plan(mask, sp, stream=None):
     return dbsp.dbsp_shard_masks(mask, sp.shard_of, sp.n_shards, stream=stream)
 
 
+def dense_lists(mask, causal=False, out=None, stream=None):
+    """(counts int32 [B,H,nQ], cols int16 [B,H,nQ,nK]): every row's dense KV blocks, for
+    ``attention(..., lists=...)``. With ``causal`` only the blocks on or below the diagonal."""
+    counts, cols = (None, None) if out is None else out
+    return dbsp.dbsp_dense_block_lists(mask, causal, counts, cols, stream=stream)
+
+
 def attention(q, k, v, mask, block, causal, p, out=None, lse=None, scale=0.0, cta_timing=None,
-              stream=None):
-    """Final-mode attention over plan ``p``; returns (out bf16, lse fp32)."""
+              stream=None, lists=None):
+    """Final-mode attention over plan ``p``; returns (out bf16, lse fp32). With ``lists``
+    (from ``dense_lists`` of the same mask and causal flag) the kernel reads each item's
+    dense blocks from them instead of scanning its mask row; the output is the same."""
     B, H, S, d = q.shape
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, block, causal, p.worker_offsets, p.worklist,
-                                    p.n_workers, out=out, lse=lse, scale=scale, cta_timing=cta_timing,
-                                    stream=stream)
+    if lists is not None:
+        dbsp.dbsp_block_sparse_attn_fwd_listed(q, k, v, mask, block, causal, p.worker_offsets, p.worklist,
+                                               p.n_workers, lists[0], lists[1], out=out, lse=lse, scale=scale,
+                                               cta_timing=cta_timing, stream=stream)
+    else:
+        dbsp.dbsp_block_sparse_attn_fwd(q, k, v, mask, block, causal, p.worker_offsets, p.worklist,
+                                        p.n_workers, out=out, lse=lse, scale=scale, cta_timing=cta_timing,
+                                        stream=stream)
     return out, lse
 
 
@@ -122,27 +136,34 @@ class PipelinedSteps:
     The attention kernel fills every SM it runs on (one persistent CTA per SM holds the
     whole register file), so a plan launched beside it would find no room. Here the
     attention runs on ``n_workers`` = SM count - 1 workers and the remaining SM takes the
-    mask loads and the LPT plan of the next batch meanwhile, on a side stream, into the
-    second of two plan buffers. ``prime`` plans the first batch; each ``step`` then runs
-    one batch's attention on ``stream`` and plans the next one beside it. The plan waits
-    for everything enqueued on ``stream`` before the step (so it never overwrites a plan
-    that an earlier attention still reads), and ``stream`` waits for the plan at the end
-    of the step. Results are those of ``plan`` + ``attention`` on each batch.
+    mask loads, the LPT plan and the dense-block lists of the next batch meanwhile, on a
+    side stream, into the second of two plan buffers. ``prime`` plans the first batch;
+    each ``step`` then runs one batch's attention on ``stream`` (reading its dense-block
+    lists) and plans the next one beside it. The plan waits for everything enqueued on
+    ``stream`` before the step (so it never overwrites a plan that an earlier attention
+    still reads), and ``stream`` waits for the plan at the end of the step. Results are
+    those of ``plan`` + ``attention`` on each batch. ``causal`` is the attention's: loads,
+    plans and lists then count only the blocks on or below the diagonal, the ones it computes.
     """
 
-    def __init__(self, B, H, nQ, nK, device, n_workers=None, causal_loads=False):
+    def __init__(self, B, H, nQ, nK, device, causal=False, n_workers=None, use_lists=True):
         self.n_workers = n_workers or max(1, default_workers(device) - 1)
         self.plans = [alloc_plan(B, H, nQ, nK, self.n_workers, device) for _ in range(2)]
-        self.causal_loads = causal_loads
+        self.causal = bool(causal)
+        self.lists = [(torch.empty((B, H, nQ), dtype=torch.int32, device=device),
+                       torch.empty((B, H, nQ, nK), dtype=torch.int16, device=device)) for _ in range(2)] \
+            if use_lists else None
         self._side = torch.cuda.Stream(device, priority=0)
         self._cur = 0
 
-    def _plan(self, mask, p, stream):
-        plan(mask, self.n_workers, out=p, stream=stream, causal=self.causal_loads)
+    def _plan(self, mask, i, stream):
+        plan(mask, self.n_workers, out=self.plans[i], stream=stream, causal=self.causal)
+        if self.lists is not None:
+            dense_lists(mask, self.causal, out=self.lists[i], stream=stream)
 
     def prime(self, mask, stream=None):
         """Plans the first batch (on ``stream``)."""
-        self._plan(mask, self.plans[self._cur], stream or torch.cuda.current_stream(mask.device))
+        self._plan(mask, self._cur, stream or torch.cuda.current_stream(mask.device))
 
     def step(self, q, k, v, mask, block, causal, next_mask=None, out=None, lse=None, scale=0.0,
              cta_timing=None, stream=None, events=None):
@@ -151,6 +172,8 @@ class PipelinedSteps:
         given, are four CUDA events recorded at the step's start, the attention's end (both
         on ``stream``), the plan's end (side stream) and the step's end (``stream``).
         Returns (out, lse)."""
+        if bool(causal) != self.causal:
+            raise ValueError("causal differs from the one the batches are planned for")
         st = stream or torch.cuda.current_stream(q.device)
         e = events or [torch.cuda.Event() for _ in range(4)]
         e[0].record(st)
@@ -160,11 +183,12 @@ class PipelinedSteps:
         if lse is None:
             lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
         attention(q, k, v, mask, block, causal, self.plans[self._cur], out=out, lse=lse, scale=scale,
-                  cta_timing=cta_timing, stream=st)
+                  cta_timing=cta_timing, stream=st,
+                  lists=None if self.lists is None else self.lists[self._cur])
         e[1].record(st)
         self._side.wait_event(e[0])
         if next_mask is not None:
-            self._plan(next_mask, self.plans[1 - self._cur], self._side)
+            self._plan(next_mask, 1 - self._cur, self._side)
         e[2].record(self._side)
         st.wait_event(e[2])
         e[3].record(st)

@@ -14,6 +14,10 @@ heads (``kv_block_loads``).
 Two versions are kept: ``block_mask_loads_loops`` walks every entry with Python
 loops (tiny masks only) and ``block_mask_loads`` uses numpy sums over ``mask != 0``.
 The tests cross-check them on mid-sized masks.
+
+``dense_block_lists`` lists each row's dense blocks themselves (the blocks a row's load
+counts), in ascending KV-block order; causal attention computes only those on or below
+the diagonal (6D notes, §2.3), so the causal lists stop there.
 """
 
 import numpy as np
@@ -62,4 +66,32 @@ def kv_block_loads(mask):
     for b in range(B):
         for h in range(H):
             out += col[b, h]
+    return out
+
+
+def dense_block_lists_loops(mask, causal=False):
+    """Each row's dense KV-block indices, ascending, by explicit loops (tiny masks only).
+
+    mask: integer array [B, H, nQ, nK]; rows r = (b*H + h)*nQ + qb. With ``causal`` only
+    the blocks j <= qb. Returns a list of int64 arrays, one per row.
+    """
+    mask = np.asarray(mask)
+    B, H, nQ, nK = mask.shape
+    rows = mask.reshape(-1, nK)
+    out = []
+    for r in range(rows.shape[0]):
+        limit = min(nK, r % nQ + 1) if causal else nK
+        out.append(np.array([j for j in range(limit) if rows[r, j] != 0], dtype=np.int64))
+    return out
+
+
+def dense_block_lists(mask, causal=False):
+    """Same as ``dense_block_lists_loops``, with numpy's flatnonzero per row."""
+    mask = np.asarray(mask)
+    B, H, nQ, nK = mask.shape
+    rows = mask.reshape(-1, nK)
+    out = []
+    for r in range(rows.shape[0]):
+        limit = min(nK, r % nQ + 1) if causal else nK
+        out.append(np.flatnonzero(rows[r, :limit]).astype(np.int64))
     return out

@@ -36,8 +36,9 @@ def _masks(w, n, seed):
     return out
 
 
+@pytest.mark.parametrize("lists", [True, False])
 @pytest.mark.parametrize("causal", [True, False])
-def test_pipelined_steps_match_serial_and_oracle(built_library, cuda_device, causal):
+def test_pipelined_steps_match_serial_and_oracle(built_library, cuda_device, causal, lists):
     w = W.custom(f"pipe_{int(causal)}", 1, 3, 6 * 128, 128, 128, causal, 7, 117, "bernoulli", p=0.5,
                  numpy_qkv=True)
     q, k, v = (t.to(DEV) for t in W.make_qkv(w, "cpu"))
@@ -46,7 +47,7 @@ def test_pipelined_steps_match_serial_and_oracle(built_library, cuda_device, cau
     rng = np.random.default_rng(9)
     qs = [q] + [torch.from_numpy(rng.standard_normal(q.shape).astype(np.float32)).to(torch.bfloat16).to(DEV)
                 for _ in range(2)]
-    pipe = P.PipelinedSteps(w.B, w.H, w.nQ, w.nK, DEV)
+    pipe = P.PipelinedSteps(w.B, w.H, w.nQ, w.nK, DEV, causal=causal, use_lists=lists)
     m = pipe.n_workers
     assert m == P.default_workers(DEV) - 1
     st = torch.cuda.Stream(DEV, priority=-1)

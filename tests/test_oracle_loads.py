@@ -118,3 +118,34 @@ def test_kv_block_loads_closed_form_and_total():
     kv2 = L.kv_block_loads(m2)
     assert kv2.sum() == (m2 != 0).sum()
     np.testing.assert_array_equal(kv2, (m2 != 0).sum(axis=(0, 1, 2)))
+
+
+def test_dense_block_lists_pins():
+    """The lists: their lengths are the row loads (the independent sums above), every
+    entry is a non-zero block in ascending order within the causal limit, the loop and
+    numpy versions agree, and the full causal mask lists exactly 0..qb in row qb."""
+    g = load_golden("loads_4x4.json")
+    mask = np.array(g["mask"], dtype=np.uint8)[None, None]
+    lists = L.dense_block_lists(mask)
+    assert [len(x) for x in lists] == g["row_loads"]
+    for i, x in enumerate(lists):
+        assert [j for j in range(4) if g["mask"][i][j] != 0] == x.tolist()
+    rng = np.random.default_rng(3)
+    for shape in [(1, 1, 1, 1), (2, 3, 7, 7), (1, 2, 16, 16), (1, 1, 9, 20)]:
+        m = (rng.random(shape) < 0.4).astype(np.uint8) * rng.integers(1, 255, shape).astype(np.uint8)
+        row, _, _ = L.block_mask_loads(m)
+        for causal in ([False, True] if shape[2] == shape[3] else [False]):
+            a = L.dense_block_lists(m, causal)
+            b = L.dense_block_lists_loops(m, causal)
+            nQ = shape[2]
+            for r, (x, y) in enumerate(zip(a, b)):
+                np.testing.assert_array_equal(x, y)
+                assert np.all(np.diff(x) > 0)
+                assert np.all(m.reshape(-1, shape[3])[r, x] != 0)
+                if causal:
+                    assert np.all(x <= r % nQ)
+            if not causal:
+                assert [len(x) for x in a] == row.reshape(-1).tolist()
+    full = np.ones((1, 1, 12, 12), dtype=np.uint8)
+    for qb, x in enumerate(L.dense_block_lists(full, causal=True)):
+        assert x.tolist() == list(range(qb + 1))
