@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one attention launch on this workload, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel source it was
 # taken on: any other attn.cu reports null.
-NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "0887dc89cc32435e", "bytes": 315.31e6}
+NCU_ATTN_TRAFFIC = {"attn_sha256_prefix": "d693011cd448583d", "bytes": 313.17e6}
 
 
 def attn_traffic():
