@@ -505,11 +505,29 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
     key[q] = p < m ? (K)p : kNone;  // load 0, worker p
     cnt[q] = 0;
   }
+  // the lane's smallest key, as a balanced tree of minimums (log2 KMAX deep)
   auto lane_min = [&]() {
-    K v = key[0];
+    K a[KMAX];
 #pragma unroll
-    for (int q = 1; q < KMAX; ++q) v = key[q] < v ? key[q] : v;
-    return v;
+    for (int q = 0; q < KMAX; ++q) a[q] = key[q];
+#pragma unroll
+    for (int step = 1; step < KMAX; step <<= 1) {
+#pragma unroll
+      for (int q = 0; q + step < KMAX; q += 2 * step) a[q] = a[q + step] < a[q] ? a[q + step] : a[q];
+    }
+    return a[0];
+  };
+  // key[idx] picked by the bits of idx, a balanced tree of selects (log2 KMAX deep)
+  auto pick = [&](int idx) {
+    K a[KMAX];
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) a[q] = key[q];
+#pragma unroll
+    for (int step = 1; step < KMAX; step <<= 1) {
+#pragma unroll
+      for (int q = 0; q + step < KMAX; q += 2 * step) a[q] = (idx & step) ? a[q + step] : a[q];
+    }
+    return a[0];
   };
   K my_min = lane_min();
   const K bonus_key = (K)bonus << kWorkerBits;
@@ -528,9 +546,7 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
       const int h = __shfl_sync(0xffffffffu, my_h, s);
       // the lane holding the home worker offers its key lowered by the bonus (branch-free:
       // every lane evaluates it, so the warp never diverges on the way to the minimum)
-      K kh = kNone;
-#pragma unroll
-      for (int q = 0; q < KMAX; ++q) kh = q == (h >> 5) ? key[q] : kh;
+      K kh = pick(h >> 5);  // (h >> 5 < KMAX for every worker; for h < 0 the value is unused)
       kh -= bonus_key;
       const K cand = (h >= 0 && (h & 31) == lane && kh < my_min) ? kh : my_min;
       int p;
