@@ -540,6 +540,7 @@ __device__ __forceinline__ void greedy_serial(const Sorted sorted, const int32_t
       if (home) my_h = home[my_i];
     }
     const int chunk = min(32, n - base);
+#pragma unroll 2  // the next item's shuffles overlap this item's chain (4 and 8 were slower)
     for (int s = 0; s < chunk; ++s) {
       const int i = __shfl_sync(0xffffffffu, my_i, s);
       const int w = __shfl_sync(0xffffffffu, my_w, s);
