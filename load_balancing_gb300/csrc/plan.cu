@@ -15,9 +15,10 @@
 //   phase 0  check loads and home, find the load range; when n <= 45056 and every
 //            load <= 2047 the loads are staged in shared memory as uint16
 //            ("staged" path), otherwise the kernel works from global memory;
-//   phase 1  the stable order (load desc, id asc): a counting sort through a
-//            shared-memory histogram, its stable scatter done by one warp with
-//            match_any (or rank-by-comparison for n <= 16384 with large loads);
+//   phase 1  the stable order (load desc, id asc): a counting sort through
+//            shared-memory histograms, its stable scatter done per warp with match_any
+//            (groups of ids of one load at once; one warp over the worklist when the
+//            loads are not staged, rank-by-comparison for n <= 16384 with large loads);
 //   phase 2  the greedy.
 //            Without a bonus (whole CTA) it goes in batches over the workers' keys sorted
 //            ascending in A: the next items take A[0], A[1], ... while A[j] stays below
@@ -50,6 +51,11 @@ constexpr int kMaxItemsCompare = 16384;
 constexpr int kWorkerBits = 11;  // worker index < 2048 in the packed key
 constexpr long long kWorkerMask = (1LL << kWorkerBits) - 1;
 constexpr long long kKeyNone = LLONG_MAX;
+constexpr int kRunLoadBits = 11;  // runs of equal load: (end << 11 | load), load <= kStagedMaxLoad
+constexpr int kRunLoadMask = (1 << kRunLoadBits) - 1;
+static_assert(kStagedMaxLoad <= kRunLoadMask && (long long)kStagedMaxItems << kRunLoadBits < (1LL << 31),
+              "a run's end and load share one int");
+static_assert(2 * DBSP_MAX_WORKERS * 2 >= kStagedMaxLoad + 1, "the run table fits the key array");
 
 constexpr size_t kStagedBytes = 2ull * kStagedMaxItems + 4ull * (kStagedMaxLoad + 2) + 4ull * 8 * (kStagedMaxLoad + 1);
 constexpr size_t kGlobalBytes = 4ull * (kMaxLoadCounting + 2 > kMaxItemsCompare ? kMaxLoadCounting + 2 : kMaxItemsCompare);
@@ -263,6 +269,11 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
 //   * bp == m with m or more items of one load left in the run: every later round of m
 //     items keeps the same order, so floor(r / m) whole rounds are placed at once and
 //     every load grows by the same amount (kept aside as a shift).
+// The load of a sorted position is read off the staged loads (sload) where they fit beside
+// the order; otherwise from a table of the runs of equal load (the non-empty load bins
+// only, run[k] = (one past the run's last position << 11 | its load)), so that finding the
+// run of a position never walks the empty bins between two loads (a handful of distinct
+// loads spread over hundreds of bins on the imbalance workload).
 // After a batch the picked workers move up in a ring of load buckets (bucket L mod R
 // holds, as a bitmask, the workers whose stored load is L; R a power of two >= 2 wmax +
 // 1, since every load stays within [L0, L0 + 2 wmax] of the minimum L0), and A is
@@ -276,7 +287,8 @@ constexpr int kWorkersPerThread = DBSP_MAX_WORKERS / kThreads;
 // pick, or more batches than items) instead of looping.
 __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads, const uint16_t* __restrict__ sorted,
                                               const uint16_t* __restrict__ sload,
-                                              const int* bin_end, int nbins, int max_load, int n, int m, int cm,
+                                              const int* bin_end, int max_load, const int* run, int n, int m,
+                                              int cm,
                                               int bc, int ic, int R, uint32_t* bkt, int* pre, int* bcnt, int* Lw,
                                               unsigned long long* A, int* counts, long long* final_load,
                                               int32_t* __restrict__ worker_of, int* red) {
@@ -318,7 +330,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
   __syncthreads();
   int L0 = 0;           // stored load of A[0]
   long long shift = 0;  // load added to every worker by whole rounds
-  int s = 0, bin = 0;
+  int s = 0, k0 = 0;  // the next item and the run holding it
   long long batches = 0;
   const long long max_batches = (long long)n + 8;
   // block-wide sum of one int per thread (uses red; synchronises)
@@ -333,14 +345,16 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
   };
   while (s < n) {
     if (++batches > max_batches) return false;
-    // the run that holds item s: read off its staged load, else walk the bins
+    int run_end, ls;  // the run holding item s: its end and load
     if (sload) {
-      bin = max_load - (int)sload[s];
+      ls = sload[s];
+      run_end = bin_end[max_load - ls];
     } else {
-      while (bin < nbins && bin_end[bin] <= s) ++bin;
+      while ((run[k0] >> kRunLoadBits) <= s) ++k0;  // (s < n, the last run's end)
+      run_end = run[k0] >> kRunLoadBits;
+      ls = run[k0] & kRunLoadMask;
     }
-    const int run_end = bin_end[bin];
-    const int ws = (max_load - bin) * bc + ic;       // planning load of item s
+    const int ws = ls * bc + ic;  // planning load of item s
     const unsigned long long key0 = A[0];
     // every stored load after this batch lies in [L0, L0 + span): the largest is at most
     // the current largest plus ws (the items are in descending order of load)
@@ -367,9 +381,9 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
         if (sload) {
           lj = sload[s + j];
         } else {
-          int b2 = bin;
-          while (bin_end[b2] <= s + j) ++b2;  // (position s + j < n = the last run's end)
-          lj = max_load - b2;
+          int k = k0;
+          while ((run[k] >> kRunLoadBits) <= s + j) ++k;  // (s + j < n, the last run's end)
+          lj = run[k] & kRunLoadMask;
         }
         wj[k] = lj * bc + ic;
         c += A[j] < key0 + ((unsigned long long)wj[k] << kWorkerBits);
@@ -755,30 +769,60 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     int* mine = whist + warp * nbins;
     // the loads of each sorted position as well, when they fit beside the order
     uint16_t* sl = n <= kStagedMaxItems / 2 ? reinterpret_cast<uint16_t*>(dyn + kStagedMaxItems) : nullptr;
-    constexpr int kC = 4;  // chunks of 32 whose loads are read ahead
-    for (int base0 = lo; base0 < hi; base0 += 32 * kC) {
-      int v[kC];
+    // groups of kC chunks of 32 ids; the next group's loads are read while this one is placed
+    constexpr int kC = 8;
+    auto fetch = [&](int base0, int (&x)[kC]) {
 #pragma unroll
       for (int u = 0; u < kC; ++u) {
         const int i = base0 + 32 * u + lane;
-        v[u] = i < hi ? __ldg(loads + i) : 0;
+        x[u] = i < hi ? __ldg(loads + i) : -1;
       }
+    };
+    int v[kC];
+    fetch(lo, v);
+    for (int base0 = lo; base0 < hi; base0 += 32 * kC) {
+      int nv[kC];
+      fetch(base0 + 32 * kC, nv);
+      // a group whose ids all carry one load (a head of equal row loads) fills consecutive
+      // positions of its bin at once
+      const int v0 = __shfl_sync(0xffffffffu, v[0], 0);  // (id base0 < hi)
+      bool one = true;
 #pragma unroll
-      for (int u = 0; u < kC; ++u) {
-        const int i = base0 + 32 * u + lane;
-        const unsigned active = __ballot_sync(0xffffffffu, i < hi);
-        if (i < hi) {
-          const int bin = max_load - v[u];
-          const unsigned peers = __match_any_sync(active, bin);
-          const unsigned below = peers & ((1u << lane) - 1);
-          const int pos = mine[bin] + __popc(below);
-          order[pos] = (uint16_t)i;
-          if (sl) sl[pos] = (uint16_t)v[u];
-          __syncwarp(active);
-          if (below == 0) mine[bin] += __popc(peers);
+      for (int u = 0; u < kC; ++u) one &= v[u] == v0 || base0 + 32 * u + lane >= hi;
+      if (__all_sync(0xffffffffu, one)) {
+        const int bin = max_load - v0;
+        const int pos0 = mine[bin];
+#pragma unroll
+        for (int u = 0; u < kC; ++u) {
+          const int i = base0 + 32 * u + lane;
+          if (i < hi) {
+            order[pos0 + 32 * u + lane] = (uint16_t)i;
+            if (sl) sl[pos0 + 32 * u + lane] = (uint16_t)v0;
+          }
         }
         __syncwarp();
+        if (lane == 0) mine[bin] = pos0 + min(32 * kC, hi - base0);
+        __syncwarp();
+      } else {
+#pragma unroll
+        for (int u = 0; u < kC; ++u) {
+          const int i = base0 + 32 * u + lane;
+          const unsigned active = __ballot_sync(0xffffffffu, i < hi);
+          if (i < hi) {
+            const int bin = max_load - v[u];
+            const unsigned peers = __match_any_sync(active, bin);
+            const unsigned below = peers & ((1u << lane) - 1);
+            const int pos = mine[bin] + __popc(below);
+            order[pos] = (uint16_t)i;
+            if (sl) sl[pos] = (uint16_t)v[u];
+            __syncwarp(active);
+            if (below == 0) mine[bin] += __popc(peers);
+          }
+          __syncwarp();
+        }
       }
+#pragma unroll
+      for (int u = 0; u < kC; ++u) v[u] = nv[u];
     }
     sload = sl;
     sorted = Sorted{order, nullptr};
@@ -832,7 +876,22 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   if (home != nullptr && bonus > 0 && (unsigned long long)bonus > sh.total_load) {
     if (tid < 32) greedy_all_home(sorted, loads, home, bc, ic, n, m, cm, counts, final_load, worker_of);
   } else if (counting && (home == nullptr || bonus == 0) && ring) {
-    if (!greedy_sorted(loads, sorted.smem, sload, bin_end, nbins, max_load, n, m, cm, bc, ic, ring_R,
+    // without staged loads, the table of runs (non-empty load bins, heaviest first) in the
+    // key array, which this path does not use: one warp compacts the bins by ballots
+    int* run = sload ? nullptr : reinterpret_cast<int*>(keys[0]);
+    if (run && tid < 32) {
+      int nr = 0;
+      for (int b0 = 0; b0 < nbins; b0 += 32) {
+        const int b = b0 + lane;
+        const int e = b < nbins ? bin_end[b] : 0;
+        const bool used = b < nbins && e > (b == 0 ? 0 : bin_end[b - 1]);
+        const unsigned ballot = __ballot_sync(0xffffffffu, used);
+        if (used) run[nr + __popc(ballot & ((1u << lane) - 1u))] = (e << kRunLoadBits) | (max_load - b);
+        nr += __popc(ballot);
+      }
+    }
+    __syncthreads();
+    if (!greedy_sorted(loads, sorted.smem, sload, bin_end, max_load, run, n, m, cm, bc, ic, ring_R,
                        reinterpret_cast<uint32_t*>(dyn + kRingOff), reinterpret_cast<int*>(dyn + kPreOff),
                        reinterpret_cast<int*>(dyn + kCntOff), reinterpret_cast<int*>(dyn + kLwOff),
                        reinterpret_cast<unsigned long long*>(dyn + kAOff), counts, final_load, worker_of, sh.scan)) {
