@@ -333,16 +333,6 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
   int s = 0, k0 = 0;  // the next item and the run holding it
   long long batches = 0;
   const long long max_batches = (long long)n + 8;
-  // block-wide sum of one int per thread (uses red; synchronises)
-  auto block_sum = [&](int x) {
-    x = __reduce_add_sync(0xffffffffu, x);
-    if (lane == 0) red[warp] = x;
-    __syncthreads();
-    int t = 0;
-#pragma unroll
-    for (int q = 0; q < kW; ++q) t += red[q];
-    return t;
-  };
   while (s < n) {
     if (++batches > max_batches) return false;
     int run_end, ls;  // the run holding item s: its end and load
@@ -368,28 +358,35 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
       s = n;
       break;
     }
-    // ---- bp: the positions j whose key is below A[0] + W(s + j)
+    // ---- bp: the positions j whose key is below A[0] + W(s + j). The predicate holds for a
+    // prefix of j (A[j] - W(s + j) grows with j), so every warp finds its end by itself,
+    // the last position first (a whole round) and then 32 positions per ballot, with no
+    // block barrier; every warp reads the same keys and loads and gets the same bp.
     const int cap = min(m, n - s);
-    int wj[kWorkersPerThread];
-    int c = 0;
-#pragma unroll
-    for (int k = 0; k < kWorkersPerThread; ++k) {
-      const int j = tid + k * kThreads;
-      wj[k] = 0;
-      if (j < cap) {
-        int lj;  // the item's load: staged, or that of the run holding position s + j
-        if (sload) {
-          lj = sload[s + j];
-        } else {
-          int k = k0;
-          while ((run[k] >> kRunLoadBits) <= s + j) ++k;  // (s + j < n, the last run's end)
-          lj = run[k] & kRunLoadMask;
+    auto wload = [&](int pos) {  // planning load of sorted position pos (s <= pos < n)
+      if (pos < run_end) return ws;
+      int l;
+      if (sload) {
+        l = sload[pos];
+      } else {
+        int k = k0 + 1;
+        while ((run[k] >> kRunLoadBits) <= pos) ++k;  // (pos < n, the last run's end)
+        l = run[k] & kRunLoadMask;
+      }
+      return l * bc + ic;
+    };
+    auto below = [&](int j) { return A[j] < key0 + ((unsigned long long)wload(s + j) << kWorkerBits); };
+    int bp = cap;
+    if (!below(cap - 1)) {
+      for (int c = 0; c < cap; c += 32) {
+        const int j = c + lane;
+        const unsigned ok = __ballot_sync(0xffffffffu, j < cap && below(j));
+        if (ok != 0xffffffffu) {
+          bp = c + __ffs(~ok) - 1;
+          break;
         }
-        wj[k] = lj * bc + ic;
-        c += A[j] < key0 + ((unsigned long long)wj[k] << kWorkerBits);
       }
     }
-    const int bp = block_sum(c);
     if (bp < 1) return false;
     if (bp == 1) {
       // ---- the minimum alone: it keeps winning while its key stays below the runner-up
@@ -437,7 +434,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
           const int c0 = counts[p];
           worker_of[sorted[s + j]] = p + cm * c0;
           counts[p] = c0 + 1;
-          const int Lo = Lw[p], Ln = Lo + wj[k];
+          const int Lo = Lw[p], Ln = Lo + wload(s + j);
           const uint32_t bit = 1u << (p & 31);
           atomicAnd(&bkt[(Lo & rmask) * WPB + (p >> 5)], ~bit);
           atomicOr(&bkt[(Ln & rmask) * WPB + (p >> 5)], bit);
