@@ -965,12 +965,17 @@ def run_kernels_once(args):
     out = torch.empty((rows, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty(rows, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
+    ni = row.numel()
+    iwo = torch.empty(ni, dtype=torch.int32, device=dev)
+    iwl = torch.empty(ni, dtype=torch.int32, device=dev)
     dbsp.dbsp_block_mask_loads(mask, row, col, head)
     dbsp.dbsp_plan_lpt(lrow, m, wo, off, wlst, wload)
+    dbsp.dbsp_plan_lpt(row.view(-1), m, iwo, off, iwl, wload)  # the imbalance workload's 40,960 items
     dbsp.dbsp_merge_partials(o, mm, ll, out, lse)
     torch.cuda.synchronize()
     status = dbsp.dbsp_device_status()
-    print(json.dumps({"profile_kernels": ["mask_loads", "lpt_plan", "merge_partials"], "device_status": status}))
+    print(json.dumps({"profile_kernels": ["mask_loads", "lpt_plan (llm)", "lpt_plan (imbalance)", "merge_partials"],
+                      "device_status": status}))
     return 0 if status == 0 else 1
 
 
