@@ -78,6 +78,15 @@ constexpr size_t kAOff = kLwOff + 4ull * DBSP_MAX_WORKERS;    // sorted keys
 constexpr size_t kRingEnd = kAOff + 8ull * DBSP_MAX_WORKERS;
 constexpr size_t kDynBytes = kDynBytes0 > kRingEnd ? kDynBytes0 : kRingEnd;
 
+// Global reads in flight per thread in phases 0, 1 and 3, as a type: 8 from kDeepItems
+// items up, 4 below. Both depths are instantiated and a launch runs one, so a small plan
+// fetches (cold) only the shorter code.
+template <int U>
+struct Depth {
+  static constexpr int value = U;
+};
+constexpr int kDeepItems = 16384;
+
 // Exclusive scan over `n` ints in shared memory `a` (in place). All threads call it.
 __device__ void block_exclusive_scan(int* a, int n, int* warp_sums) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -281,10 +290,11 @@ __device__ void greedy_batched(const Sorted sorted, const int* bin_end, int nbin
 // lower buckets (an exclusive scan of the bucket counts from L0) plus the workers below
 // it in its own bucket.
 constexpr int kRingWords = kRingWordsMax;  // R * ceil(m / 32) bucket words
-constexpr int kWorkersPerThread = DBSP_MAX_WORKERS / kThreads;
 
-// Returns false (uniformly) when the state is found inconsistent (a batch without a
-// pick, or more batches than items) instead of looping.
+// WPT = ceil(m_max / 256) workers per thread for the instantiation's worker bound. Returns
+// false (uniformly) when the state is found inconsistent (a batch without a pick, or
+// more batches than items) instead of looping.
+template <int WPT>
 __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads, const uint16_t* __restrict__ sorted,
                                               const uint16_t* __restrict__ sload,
                                               const int* bin_end, int max_load, const int* run, int n, int m,
@@ -411,7 +421,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
       // ---- whole rounds of equal loads: the order of A does not change
       const int F = (run_end - s) / m;
 #pragma unroll
-      for (int k = 0; k < kWorkersPerThread; ++k) {
+      for (int k = 0; k < WPT; ++k) {
         const int j = tid + k * kThreads;
         if (j < m) {
           const int p = (int)(A[j] & kWorkerMask);
@@ -427,7 +437,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
     } else {
       // ---- a batch: item s + j to worker A[j] for j < bp; each moves up by W(s + j)
 #pragma unroll
-      for (int k = 0; k < kWorkersPerThread; ++k) {
+      for (int k = 0; k < WPT; ++k) {
         const int j = tid + k * kThreads;
         if (j < bp) {
           const int p = (int)(A[j] & kWorkerMask);
@@ -472,7 +482,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
     __syncthreads();
     int bad = 0;  // a load outside [L0, L0 + span) or a position outside [0, m): inconsistent state
 #pragma unroll
-    for (int k = 0; k < kWorkersPerThread; ++k) {
+    for (int k = 0; k < WPT; ++k) {
       const int p = tid + k * kThreads;
       if (p < m) {
         const int L = Lw[p];
@@ -645,49 +655,56 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   __syncthreads();
   int lmin = INT_MAX, lmax = INT_MIN, badh = 0;
   unsigned long long tot = 0;
-  constexpr int kU = 8;  // global reads in flight per thread
   const bool vec4 = ((reinterpret_cast<uintptr_t>(loads) | reinterpret_cast<uintptr_t>(home)) & 15u) == 0;
   const int n4 = vec4 ? n / 4 : 0;  // items [0, 4 n4) read as int4
-  for (int base = tid; base < n4; base += kU * kThreads) {
-    int4 v[kU], hv[kU];
+  const bool deep = n >= kDeepItems;
+  auto validate = [&](auto depth) {
+    constexpr int kU = decltype(depth)::value;
+    for (int base = tid; base < n4; base += kU * kThreads) {
+      int4 v[kU], hv[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = base + u * kThreads;
-      v[u] = i < n4 ? __ldg(reinterpret_cast<const int4*>(loads) + i) : make_int4(0, 0, 0, 0);
-      hv[u] = (home && i < n4) ? __ldg(reinterpret_cast<const int4*>(home) + i) : make_int4(0, 0, 0, 0);
-    }
+      for (int u = 0; u < kU; ++u) {
+        const int i = base + u * kThreads;
+        v[u] = i < n4 ? __ldg(reinterpret_cast<const int4*>(loads) + i) : make_int4(0, 0, 0, 0);
+        hv[u] = (home && i < n4) ? __ldg(reinterpret_cast<const int4*>(home) + i) : make_int4(0, 0, 0, 0);
+      }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (base + u * kThreads < n4) {
-        const int w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        const int h4[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+      for (int u = 0; u < kU; ++u) {
+        if (base + u * kThreads < n4) {
+          const int w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          const int h4[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          lmin = min(lmin, w4[e]); lmax = max(lmax, w4[e]);
-          tot += (unsigned long long)max(w4[e], 0) * (unsigned long long)bc + (unsigned long long)ic;
-          badh |= (h4[e] < 0 || h4[e] >= m);
+          for (int e = 0; e < 4; ++e) {
+            lmin = min(lmin, w4[e]); lmax = max(lmax, w4[e]);
+            tot += (unsigned long long)max(w4[e], 0) * (unsigned long long)bc + (unsigned long long)ic;
+            badh |= (h4[e] < 0 || h4[e] >= m);
+          }
         }
       }
     }
-  }
-  for (int base = 4 * n4 + tid; base < n; base += kU * kThreads) {
-    int v[kU], hv[kU];
+    for (int base = 4 * n4 + tid; base < n; base += kU * kThreads) {
+      int v[kU], hv[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = base + u * kThreads;
-      v[u] = i < n ? __ldg(loads + i) : 0;
-      hv[u] = (home && i < n) ? __ldg(home + i) : 0;
-    }
+      for (int u = 0; u < kU; ++u) {
+        const int i = base + u * kThreads;
+        v[u] = i < n ? __ldg(loads + i) : 0;
+        hv[u] = (home && i < n) ? __ldg(home + i) : 0;
+      }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (base + u * kThreads < n) {
-        const int w = v[u];
-        lmin = min(lmin, w); lmax = max(lmax, w);
-        tot += (unsigned long long)max(w, 0) * (unsigned long long)bc + (unsigned long long)ic;
-        badh |= (hv[u] < 0 || hv[u] >= m);
+      for (int u = 0; u < kU; ++u) {
+        if (base + u * kThreads < n) {
+          const int w = v[u];
+          lmin = min(lmin, w); lmax = max(lmax, w);
+          tot += (unsigned long long)max(w, 0) * (unsigned long long)bc + (unsigned long long)ic;
+          badh |= (hv[u] < 0 || hv[u] >= m);
+        }
       }
     }
-  }
+  };
+  if (deep)
+    validate(Depth<8>{});
+  else
+    validate(Depth<4>{});
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   if (lane == 0) atomicAdd(&sh.total_load, tot);  // one atomic per warp
@@ -733,22 +750,29 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
     const int vlo = vec4 ? min(hi, (lo + 3) & ~3) : hi, vhi = vec4 ? max(vlo, hi & ~3) : hi;
     for (int i = lo + lane; i < vlo; i += 32) atomicAdd(&whist[warp * nbins + (max_load - __ldg(loads + i))], 1);
     for (int i = vhi + lane; i < hi; i += 32) atomicAdd(&whist[warp * nbins + (max_load - __ldg(loads + i))], 1);
-    for (int base = vlo / 4 + lane; base < vhi / 4; base += 32 * kU) {
-      int4 v[kU];
+    auto histogram = [&](auto depth) {
+      constexpr int kU = decltype(depth)::value;
+      for (int base = vlo / 4 + lane; base < vhi / 4; base += 32 * kU) {
+        int4 v[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u)
-        v[u] = base + 32 * u < vhi / 4 ? __ldg(reinterpret_cast<const int4*>(loads) + base + 32 * u)
-                                       : make_int4(-1, -1, -1, -1);
+        for (int u = 0; u < kU; ++u)
+          v[u] = base + 32 * u < vhi / 4 ? __ldg(reinterpret_cast<const int4*>(loads) + base + 32 * u)
+                                         : make_int4(-1, -1, -1, -1);
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if (v[u].x >= 0) {
-          atomicAdd(&whist[warp * nbins + (max_load - v[u].x)], 1);
-          atomicAdd(&whist[warp * nbins + (max_load - v[u].y)], 1);
-          atomicAdd(&whist[warp * nbins + (max_load - v[u].z)], 1);
-          atomicAdd(&whist[warp * nbins + (max_load - v[u].w)], 1);
+        for (int u = 0; u < kU; ++u) {
+          if (v[u].x >= 0) {
+            atomicAdd(&whist[warp * nbins + (max_load - v[u].x)], 1);
+            atomicAdd(&whist[warp * nbins + (max_load - v[u].y)], 1);
+            atomicAdd(&whist[warp * nbins + (max_load - v[u].z)], 1);
+            atomicAdd(&whist[warp * nbins + (max_load - v[u].w)], 1);
+          }
         }
       }
-    }
+    };
+    if (deep)
+      histogram(Depth<8>{});
+    else
+      histogram(Depth<4>{});
     __syncthreads();
     for (int b = tid; b <= nbins; b += kThreads) {
       int t = 0;
@@ -888,7 +912,8 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
       }
     }
     __syncthreads();
-    if (!greedy_sorted(loads, sorted.smem, sload, bin_end, max_load, run, n, m, cm, bc, ic, ring_R,
+    constexpr int WPT = (KMAX * 32 + kThreads - 1) / kThreads;
+    if (!greedy_sorted<WPT>(loads, sorted.smem, sload, bin_end, max_load, run, n, m, cm, bc, ic, ring_R,
                        reinterpret_cast<uint32_t*>(dyn + kRingOff), reinterpret_cast<int*>(dyn + kPreOff),
                        reinterpret_cast<int*>(dyn + kCntOff), reinterpret_cast<int*>(dyn + kLwOff),
                        reinterpret_cast<unsigned long long*>(dyn + kAOff), counts, final_load, worker_of, sh.scan)) {
@@ -935,44 +960,51 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   // per item (imbalance workload, 40,960 items: 180 -> 166 us).
   int* ws = n >= 8192 && (size_t)n * sizeof(int) <= kDynBytes ? reinterpret_cast<int*>(dyn) : nullptr;
   int32_t* wdst = ws ? ws : worklist;
-  for (int base = tid; base < nw4; base += kU * kThreads) {
-    int4 c4[kU];
+  auto scatter = [&](auto depth) {
+    constexpr int kU = decltype(depth)::value;
+    for (int base = tid; base < nw4; base += kU * kThreads) {
+      int4 c4[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      c4[u] = base + u * kThreads < nw4 ? reinterpret_cast<const int4*>(worker_of)[base + u * kThreads]
-                                        : make_int4(0, 0, 0, 0);
+      for (int u = 0; u < kU; ++u)
+        c4[u] = base + u * kThreads < nw4 ? reinterpret_cast<const int4*>(worker_of)[base + u * kThreads]
+                                          : make_int4(0, 0, 0, 0);
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i4 = base + u * kThreads;
-      if (i4 < nw4) {
-        const int cc[4] = {c4[u].x, c4[u].y, c4[u].z, c4[u].w};
-        int pp[4];
+      for (int u = 0; u < kU; ++u) {
+        const int i4 = base + u * kThreads;
+        if (i4 < nw4) {
+          const int cc[4] = {c4[u].x, c4[u].y, c4[u].z, c4[u].w};
+          int pp[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int p = cm == DBSP_MAX_WORKERS ? (cc[e] & (DBSP_MAX_WORKERS - 1)) : cc[e] % m;
-          const int rank = cm == DBSP_MAX_WORKERS ? (cc[e] >> 10) : cc[e] / m;
-          wdst[counts[p] + rank] = 4 * i4 + e;
-          pp[e] = p;
+          for (int e = 0; e < 4; ++e) {
+            const int p = cm == DBSP_MAX_WORKERS ? (cc[e] & (DBSP_MAX_WORKERS - 1)) : cc[e] % m;
+            const int rank = cm == DBSP_MAX_WORKERS ? (cc[e] >> 10) : cc[e] / m;
+            wdst[counts[p] + rank] = 4 * i4 + e;
+            pp[e] = p;
+          }
+          reinterpret_cast<int4*>(worker_of)[i4] = make_int4(pp[0], pp[1], pp[2], pp[3]);
         }
-        reinterpret_cast<int4*>(worker_of)[i4] = make_int4(pp[0], pp[1], pp[2], pp[3]);
       }
     }
-  }
-  for (int base = 4 * nw4 + tid; base < n; base += kU * kThreads) {
-    int code[kU];
+    for (int base = 4 * nw4 + tid; base < n; base += kU * kThreads) {
+      int code[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) code[u] = base + u * kThreads < n ? worker_of[base + u * kThreads] : 0;
+      for (int u = 0; u < kU; ++u) code[u] = base + u * kThreads < n ? worker_of[base + u * kThreads] : 0;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int i = base + u * kThreads;
-      if (i < n) {
-        const int p = cm == DBSP_MAX_WORKERS ? (code[u] & (DBSP_MAX_WORKERS - 1)) : code[u] % m;
-        const int rank = cm == DBSP_MAX_WORKERS ? (code[u] >> 10) : code[u] / m;
-        wdst[counts[p] + rank] = i;
-        worker_of[i] = p;
+      for (int u = 0; u < kU; ++u) {
+        const int i = base + u * kThreads;
+        if (i < n) {
+          const int p = cm == DBSP_MAX_WORKERS ? (code[u] & (DBSP_MAX_WORKERS - 1)) : code[u] % m;
+          const int rank = cm == DBSP_MAX_WORKERS ? (code[u] >> 10) : code[u] / m;
+          wdst[counts[p] + rank] = i;
+          worker_of[i] = p;
+        }
       }
     }
-  }
+  };
+  if (deep)
+    scatter(Depth<8>{});
+  else
+    scatter(Depth<4>{});
   if (ws) {
     __syncthreads();
     const bool lvec = (reinterpret_cast<uintptr_t>(worklist) & 15u) == 0;

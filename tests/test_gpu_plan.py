@@ -288,3 +288,38 @@ def test_worklist_assembled_in_shared_memory(built_library, cuda_device, n, hi, 
     rng = np.random.default_rng(n)
     loads = rng.integers(0, hi, n)
     _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+
+
+def _runs_in_id_order(rng, n, values):
+    """Loads in runs of one value in id order, of random lengths (1 to 700), so that the
+    stable scatter's groups of 256 ids meet runs that start and end mid-group."""
+    out = np.empty(n, dtype=np.int64)
+    i = 0
+    while i < n:
+        r = int(rng.integers(1, 700))
+        out[i:i + r] = rng.choice(values)
+        i += r
+    return out
+
+
+@pytest.mark.parametrize("n", [22528, 22529, 30000, 45056])
+@pytest.mark.parametrize("m", [7, 152, 1024])
+@pytest.mark.parametrize("shape", ["spread", "sparse", "id_runs"])
+def test_staged_plans_with_many_or_few_runs(built_library, cuda_device, n, m, shape):
+    """Staged plans on both sides of the 22,528-item limit for keeping the sorted loads:
+    beyond it a position's load comes from the table of runs of equal load. Loads spread
+    over [0, 2047] (short runs, few empty bins), a handful of loads far apart (long runs,
+    hundreds of empty bins between them) and runs of one load in id order (the scatter's
+    groups of one load) all give the oracle's LPT."""
+    rng = np.random.default_rng(n * 7 + m)
+    # the largest load that keeps the bucket ring (R >= 2 wmax + 1 buckets, R a power of two:
+    # R <= 4,096 and R * ceil(m / 32) <= 10,240 words), which the table of runs serves
+    wmax = {7: 2047, 152: 1023, 1024: 127}[m]
+    if shape == "spread":
+        loads = rng.integers(0, wmax + 1, n)
+    elif shape == "sparse":
+        loads = rng.choice(np.array([0, 3, wmax // 4, wmax // 2 + 1, wmax]), n)
+    else:
+        loads = _runs_in_id_order(rng, n, rng.integers(0, wmax + 1, 40))
+    loads[n // 3] = wmax
+    _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
