@@ -22,7 +22,8 @@
 //   phase 2  the greedy.
 //            Without a bonus (whole CTA) it goes in batches over the workers' keys sorted
 //            ascending in A: the next items take A[0], A[1], ... while A[j] stays below
-//            A[0] + W(s + j), exactly the one-at-a-time greedy's picks, then A is rebuilt
+//            A[0] + W(s + j), exactly the one-at-a-time greedy's picks (every warp finds
+//            the end of the batch by ballots, without a block barrier), then A is rebuilt
 //            by a counting sort over a ring of load buckets (when the loads are staged
 //            and small), else the re-keyed keys are merged back by binary searches.
 //            With a bonus (one warp) the key of item i's home worker is lowered by the
@@ -34,7 +35,9 @@
 //            (or m when ranks could reach 2^21);
 //   phase 3  CSR offsets by a block scan of the per-worker counts, then the
 //            scatter of every item to offsets[worker] + rank.
-// Global working storage is the output arrays only.
+// Phases 0, 1 and 3 keep 8 global reads in flight per thread from 16,384 items up and 4
+// below; a launch runs one of the two instantiations. Global working storage is the
+// output arrays only.
 #include <algorithm>
 #include <climits>
 
