@@ -661,6 +661,17 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_plan_kernel(
   const bool vec4 = ((reinterpret_cast<uintptr_t>(loads) | reinterpret_cast<uintptr_t>(home)) & 15u) == 0;
   const int n4 = vec4 ? n / 4 : 0;  // items [0, 4 n4) read as int4
   const bool deep = n >= kDeepItems;
+  // a large plan reads its loads (and homes) from DRAM in several rounds of reads in
+  // flight: one bulk L2 prefetch of each array first pays the latency once
+  if (deep && vec4 && tid == 0) {
+    constexpr uint32_t kChunk = 1u << 16;
+    const uint32_t bytes = (uint32_t)n4 * 16u;
+    for (uint32_t o = 0; o < bytes; o += kChunk) {
+      const uint32_t len = min(kChunk, bytes - o);
+      dbsp::ptx::bulk_prefetch_l2(reinterpret_cast<const char*>(loads) + o, len);
+      if (home) dbsp::ptx::bulk_prefetch_l2(reinterpret_cast<const char*>(home) + o, len);
+    }
+  }
   auto validate = [&](auto depth) {
     constexpr int kU = decltype(depth)::value;
     for (int base = tid; base < n4; base += kU * kThreads) {
