@@ -323,3 +323,33 @@ def test_staged_plans_with_many_or_few_runs(built_library, cuda_device, n, m, sh
         loads = _runs_in_id_order(rng, n, rng.integers(0, wmax + 1, 40))
     loads[n // 3] = wmax
     _assert_same(_plan(loads, m), OP.lpt_plan(loads, m))
+
+
+@pytest.mark.parametrize("n", [16383, 16384, 20001])
+def test_large_plans_with_homes_and_unaligned_loads(built_library, cuda_device, n):
+    """From 16,384 items up the kernel keeps 8 reads in flight per thread and prefetches
+    the loads and homes into L2 (16-byte aligned arrays only). Plans with homes and a
+    bonus, and plans whose loads start 4 bytes past a 16-byte boundary (no prefetch, no
+    16-byte reads), on both sides of that limit, are the oracle's."""
+    from load_balancing_gb300 import dbsp
+
+    rng = np.random.default_rng(n)
+    m = 152
+    loads = rng.integers(0, 90, n)
+    home = rng.integers(0, m, n)
+    for bonus in (0, 3):
+        _assert_same(_plan(loads, m, home, bonus), OP.lpt_plan(loads, m, home, bonus))
+    dev = torch.device("cuda:0")
+    buf = torch.zeros(n + 1, dtype=torch.int32, device=dev)
+    buf[1:] = torch.as_tensor(loads.astype(np.int32)).to(dev)
+    shifted = buf[1:]  # 4-byte aligned only
+    assert shifted.data_ptr() % 16 != 0
+    wo = torch.full((n,), -5, dtype=torch.int32, device=dev)
+    off = torch.full((m + 1,), -5, dtype=torch.int32, device=dev)
+    wl = torch.full((n,), -5, dtype=torch.int32, device=dev)
+    wload = torch.full((m,), -5, dtype=torch.int64, device=dev)
+    dbsp.dbsp_plan_lpt(shifted, m, wo, off, wl, wload)
+    assert dbsp.dbsp_device_status() == 0
+    got = {"worker_of": wo.cpu().numpy(), "offsets": off.cpu().numpy(), "worklist": wl.cpu().numpy(),
+           "worker_loads": wload.cpu().numpy()}
+    _assert_same(got, OP.lpt_plan(loads, m))
