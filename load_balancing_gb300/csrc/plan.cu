@@ -429,6 +429,7 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
         if (j < m) {
           const int p = (int)(A[j] & kWorkerMask);
           const int c0 = counts[p];
+#pragma unroll 4  // the order reads of several rounds go out together
           for (int f = 0; f < F; ++f) worker_of[sorted[s + f * m + j]] = p + cm * (c0 + f);
           counts[p] = c0 + F;
         }
