@@ -206,3 +206,40 @@ def test_shard_masks_host_validation(built_library, args, expect):
     from load_balancing_gb300 import dbsp
 
     assert dbsp.library().dbsp_shard_masks(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, 1, 2, 4, 4, 0, FAKE, FAKE, None), 1),               # no mask
+    ((FAKE, 0, 2, 4, 4, 0, FAKE, FAKE, None), 1),               # B < 1
+    ((FAKE, 1, 2, 4, 6, 1, FAKE, FAKE, None), 1),               # causal needs nQ == nK
+    ((FAKE, 4, 4, 46341, 46341, 0, FAKE, FAKE, None), 1),       # mask bytes overflow int
+    ((FAKE, 1, 1, 4, 65537, 0, FAKE, FAKE, None), 2),           # column indices are 16-bit
+    ((FAKE, 1, 2, 4, 4, 0, FAKE + 2, FAKE, None), 1),           # counts not 4-byte aligned
+    ((FAKE, 1, 2, 4, 4, 0, FAKE, FAKE + 1, None), 1),           # cols not 2-byte aligned
+    ((FAKE, 1, 2, 4, 4, 0, None, FAKE, None), 1),               # no counts
+])
+def test_dense_block_lists_host_validation(built_library, args, expect):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_dense_block_lists(*args) == expect
+
+
+def _listed_args(dense_n=FAKE, dense_cols=FAKE, **kw):
+    a = list(_attn_args(**kw))
+    # the listed entry takes the lists after n_workers (q .. nw are the first 14 arguments)
+    return tuple(a[:14] + [dense_n, dense_cols] + a[14:])
+
+
+@pytest.mark.parametrize("lists,kw,expect", [
+    (dict(dense_n=None), {}, 1),
+    (dict(dense_cols=None), {}, 1),
+    (dict(dense_n=FAKE + 2), {}, 1),                 # counts not 4-byte aligned
+    (dict(dense_cols=FAKE + 1), {}, 1),              # indices not 2-byte aligned
+    ({}, dict(q=None), 1),                           # the attention's own checks follow
+    ({}, dict(d=96), 2),
+    ({}, dict(out=None), 1),
+])
+def test_listed_attention_host_validation(built_library, lists, kw, expect):
+    from load_balancing_gb300 import dbsp
+
+    assert dbsp.library().dbsp_block_sparse_attn_fwd_listed(*_listed_args(**lists, **kw)) == expect
