@@ -142,3 +142,28 @@ def test_out_of_range_lists_are_reported(built_library, cuda_device):
     assert dbsp.dbsp_device_status() == dbsp.DBSP_OK
     o_ref, lse_ref = A.attention(to64(q), to64(k), to64(v), mask_np, w.block, True)
     assert_rows_close(to64(out), o_ref, to64(lse), lse_ref, what="listed after the bad lists")
+
+
+@pytest.mark.parametrize("kind", ["empty", "dense", "one_block"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("block,d", [(128, 128), (64, 64)])
+def test_listed_attention_degenerate_masks(built_library, cuda_device, kind, causal, block, d):
+    """Degenerate masks through the listed producers: every item empty (the producers
+    write O = 0 and LSE = -inf, and no MMA runs at all), every block dense, and a sequence
+    of a single block (nQ = nK = 1). Bit-identical to the scanning kernel and, element by
+    element, the oracle's."""
+    nb = 1 if kind == "one_block" else 4
+    B, H = 2, 3
+    mask_np = (np.zeros if kind == "empty" else np.ones)((B, H, nb, nb), dtype=np.uint8)
+    rng = np.random.default_rng(nb * 10 + int(causal) + block)
+    shape = (B, H, nb * block, d)
+    q, k, v = (torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16) for _ in range(3))
+    mask = torch.from_numpy(mask_np).to(DEV)
+    p = P.plan(mask, 5, causal=causal)
+    out0, lse0, out1, lse1 = _run_both(q.to(DEV), k.to(DEV), v.to(DEV), mask, block, causal, p,
+                                       P.dense_lists(mask, causal))
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    o_ref, lse_ref = A.attention(to64(q), to64(k), to64(v), mask_np, block, causal)
+    assert_rows_close(to64(out1), o_ref, to64(lse1), lse_ref, what=f"listed {kind} c{causal} b{block}")
+    if kind == "empty":
+        assert not out1.any() and torch.isneginf(lse1).all()
