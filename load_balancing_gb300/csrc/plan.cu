@@ -301,8 +301,8 @@ template <int WPT>
 __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads, const uint16_t* __restrict__ sorted,
                                               const uint16_t* __restrict__ sload,
                                               const int* bin_end, int max_load, const int* run, int n, int m,
-                                              int cm,
-                                              int bc, int ic, int R, uint32_t* bkt, int* pre, int* bcnt, int* Lw,
+                                              int cm, int bc, int ic, int R, uint32_t* bkt, int* pre, int* bcnt,
+                                              int* Lw,
                                               unsigned long long* A, int* counts, long long* final_load,
                                               int32_t* __restrict__ worker_of, int* red) {
   constexpr int kW = kThreads / 32;
