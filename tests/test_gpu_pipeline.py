@@ -73,3 +73,21 @@ def test_pipelined_steps_match_serial_and_oracle(built_library, cuda_device, cau
         assert torch.equal(outs[i][0], o_ser) and torch.equal(outs[i][1], l_ser)
         o_ref, lse_ref = A.attention(to64(qs[i]), to64(k), to64(v), masks_np[i], w.block, w.causal)
         assert_rows_close(to64(outs[i][0]), o_ref, to64(outs[i][1]), lse_ref, what=f"pipelined step {i}")
+
+
+def test_pipelined_step_rejects_a_different_causal_flag(built_library, cuda_device):
+    """The batches are planned (loads, LPT, lists) for one causal setting; a step asked
+    for the other raises before it launches anything, and the pipeline stays usable."""
+    w = W.custom("pipe_flag", 1, 2, 3 * 128, 128, 128, True, 8, 118, "bernoulli", p=0.5, numpy_qkv=True)
+    q, k, v = (t.to(DEV) for t in W.make_qkv(w, "cpu"))
+    mask_np = W.make_mask(w)
+    mask = torch.from_numpy(mask_np).to(DEV)
+    pipe = P.PipelinedSteps(w.B, w.H, w.nQ, w.nK, DEV, causal=True)
+    pipe.prime(mask)
+    with pytest.raises(ValueError):
+        pipe.step(q, k, v, mask, w.block, False)
+    o, l = pipe.step(q, k, v, mask, w.block, True)
+    torch.cuda.synchronize()
+    assert dbsp.dbsp_device_status() == 0
+    o_ref, lse_ref = A.attention(to64(q), to64(k), to64(v), mask_np, w.block, True)
+    assert_rows_close(to64(o), o_ref, to64(l), lse_ref, what="pipelined step after a rejected flag")
