@@ -496,7 +496,9 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
         }
         const uint32_t* wd = bkt + (L & rmask) * WPB;
         int pos = pre[L - L0];
-        for (int q = 0; q < (p >> 5); ++q) pos += __popc(wd[q]);
+#pragma unroll  // the words below p's word, as independent predicated reads
+        for (int q = 0; q < WPT * kThreads / 32 - 1; ++q)
+          if (q < (p >> 5)) pos += __popc(wd[q]);
         pos += __popc(wd[p >> 5] & ((1u << (p & 31)) - 1u));
         if ((unsigned)pos >= (unsigned)m) {
           bad = 1;
