@@ -462,26 +462,41 @@ __device__ __forceinline__ bool greedy_sorted(const int32_t* __restrict__ loads,
     __syncthreads();  // the buckets are final for this batch
     // ---- counting sort: exclusive scan of the bucket counts from L0 over the span
     {
+      // each thread scans a slice of at most kRingMax / kThreads buckets: its counts are
+      // read as independent predicated loads into registers (a short and a long form)
       const int per = (span + kThreads - 1) / kThreads;
-      const int i0 = min(span, tid * per), i1 = min(span, i0 + per);
-      int tot = 0;
-      for (int i = i0; i < i1; ++i) tot += bcnt[(L0 + i) & rmask];
-      int incl = tot;
+      const int i0 = min(span, tid * per), cnt = min(span, i0 + per) - i0;
+      auto scan_slice = [&](auto depth) {
+        constexpr int kN = decltype(depth)::value;
+        int c[kN];
+        int tot = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) red[warp] = incl;
-      __syncthreads();
-      int run = incl - tot;
+        for (int u = 0; u < kN; ++u) {
+          c[u] = u < cnt ? bcnt[(L0 + i0 + u) & rmask] : 0;
+          tot += c[u];
+        }
+        int incl = tot;
 #pragma unroll
-      for (int q = 0; q < kW; ++q) run += q < warp ? red[q] : 0;
-      for (int i = i0; i < i1; ++i) {
-        const int t = bcnt[(L0 + i) & rmask];
-        pre[i] = run;
-        run += t;
-      }
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) red[warp] = incl;
+        __syncthreads();
+        int run = incl - tot;
+#pragma unroll
+        for (int q = 0; q < kW; ++q) run += q < warp ? red[q] : 0;
+#pragma unroll
+        for (int u = 0; u < kN; ++u) {
+          if (u < cnt) pre[i0 + u] = run;
+          run += c[u];
+        }
+      };
+      static_assert(kRingMax / kThreads <= 16, "a thread's slice of the ring fits the long form");
+      if (per <= 2)
+        scan_slice(Depth<2>{});
+      else
+        scan_slice(Depth<16>{});
     }
     __syncthreads();
     int bad = 0;  // a load outside [L0, L0 + span) or a position outside [0, m): inconsistent state
